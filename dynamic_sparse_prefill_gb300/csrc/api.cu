@@ -1,0 +1,440 @@
+// api.cu -- the C ABI (include/crisp.h): context and workspace, argument validation,
+// TMA tensor maps, and the launch sequence of the CRISP path.  Host code only; every
+// step of the path runs in the library's kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace crisp {
+cudaError_t init_patsearch_attributes();
+cudaError_t init_attention_attributes();
+}  // namespace crisp
+
+using namespace crisp;
+
+namespace {
+
+void set_err(crisp_ctx ctx, const char* what, cudaError_t e) {
+  if (ctx) snprintf(ctx->last_err, sizeof(ctx->last_err), "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool dims_valid(const crisp_dims* d) {
+  return d && d->batch >= 1 && d->n >= 1 && d->hq >= 1 && d->hkv >= 1 && d->d >= 1 &&
+         d->hq % d->hkv == 0;
+}
+
+crisp_status check_dims(const crisp_dims* d) {
+  if (!dims_valid(d)) return CRISP_ERR_INVALID_ARG;
+  if (d->d != kD) return CRISP_ERR_UNSUPPORTED;
+  if (d->n % kBlk != 0 || d->n < kBlk || d->n > (1 << 20)) return CRISP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->batch) * d->hq > 65535) return CRISP_ERR_UNSUPPORTED;
+  return CRISP_OK;
+}
+
+crisp_status check_cfg(const crisp_cfg* c) {
+  if (!c) return CRISP_ERR_INVALID_ARG;
+  if (c->B != kBlk || c->b != kBlk) return CRISP_ERR_UNSUPPORTED;
+  if (c->w_sink < 1 || c->w_sink > kBlk || c->w_local < 1 || c->w_local > kBlk)
+    return CRISP_ERR_UNSUPPORTED;
+  if (!(c->gamma > 0.f && c->gamma <= 1.f)) return CRISP_ERR_INVALID_ARG;
+  if (!(c->alpha >= 0.f) || c->k_min_tokens < 0) return CRISP_ERR_INVALID_ARG;
+  if (!(c->tau_proxy == c->tau_proxy)) return CRISP_ERR_INVALID_ARG;
+  if ((c->flags & CRISP_FLAG_FORCE_VS) && (c->flags & CRISP_FLAG_FORCE_PE))
+    return CRISP_ERR_INVALID_ARG;
+  return CRISP_OK;
+}
+
+bool fits(const crisp_ctx ctx, const crisp_dims* d) {
+  const int64_t H = static_cast<int64_t>(d->batch) * d->hq;
+  const int64_t Hkv = static_cast<int64_t>(d->batch) * d->hkv;
+  return H <= ctx->max_H && Hkv <= ctx->max_Hkv && d->n / kBlk <= ctx->max_nb &&
+         H * (d->n / kBlk) <= ctx->max_H * ctx->max_nb;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+crisp_status make_map(crisp_ctx ctx, CUtensorMap* map, const void* base, int64_t rows) {
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kD) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                           gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(ctx->last_err, sizeof(ctx->last_err), "cuTensorMapEncodeTiled failed (%d)",
+             static_cast<int>(r));
+    return CRISP_ERR_CUDA;
+  }
+  return CRISP_OK;
+}
+
+crisp_status launched(crisp_ctx ctx, cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return CRISP_OK;
+  set_err(ctx, what, e);
+  return CRISP_ERR_CUDA;
+}
+
+crisp_status check_common(crisp_ctx ctx, const crisp_dims* dims) {
+  if (!ctx) return CRISP_ERR_INVALID_ARG;
+  crisp_status st = check_dims(dims);
+  if (st != CRISP_OK) return st;
+  if (!fits(ctx, dims)) return CRISP_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != ctx->device) return CRISP_ERR_INVALID_ARG;
+  return CRISP_OK;
+}
+
+}  // namespace
+
+namespace crisp {
+Shape make_shape(const crisp_dims& d) {
+  Shape s;
+  s.n = d.n;
+  s.nb = d.n / kBlk;
+  s.nbw = (s.nb + 31) / 32;
+  s.H = d.batch * d.hq;
+  s.Hkv = d.batch * d.hkv;
+  s.hq = d.hq;
+  s.hkv = d.hkv;
+  s.group = d.hq / d.hkv;
+  return s;
+}
+}  // namespace crisp
+
+extern "C" {
+
+crisp_cfg crisp_cfg_default(void) {
+  crisp_cfg c;
+  c.B = 128;
+  c.b = 128;
+  c.w_sink = 128;
+  c.w_local = 128;
+  c.k_min_tokens = 1024;
+  c.tau_proxy = 0.2f;
+  c.alpha = 1.0f;
+  c.gamma = 0.95f;
+  c.flags = 0;
+  return c;
+}
+
+const char* crisp_status_string(crisp_status s) {
+  switch (s) {
+    case CRISP_OK: return "ok";
+    case CRISP_ERR_INVALID_ARG: return "invalid argument";
+    case CRISP_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case CRISP_ERR_NO_MEMORY: return "device allocation failed";
+    case CRISP_ERR_CUDA: return "CUDA error";
+    case CRISP_ERR_TIMEOUT: return "device wait timed out";
+    case CRISP_ERR_DEVICE_ASSERT: return "device range check failed";
+    case CRISP_ERR_NO_SELECTION: return "no selection for these dims";
+  }
+  return "unknown status";
+}
+
+crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
+  if (!out) return CRISP_ERR_INVALID_ARG;
+  *out = nullptr;
+  crisp_status st = check_dims(max_dims);
+  if (st != CRISP_OK) return st;
+  crisp_ctx ctx = new (std::nothrow) crisp_ctx_s();
+  if (!ctx) return CRISP_ERR_NO_MEMORY;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) {
+    delete ctx;
+    return CRISP_ERR_CUDA;
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, ctx->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
+  cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (major != 10 || minor != 3) {  // the kernels are built for sm_103a only
+    delete ctx;
+    return CRISP_ERR_UNSUPPORTED;
+  }
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete ctx;
+    return CRISP_ERR_CUDA;
+  }
+  ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  if (init_patsearch_attributes() != cudaSuccess || init_attention_attributes() != cudaSuccess) {
+    delete ctx;
+    return CRISP_ERR_CUDA;
+  }
+  ctx->maxd = *max_dims;
+  const int64_t H = static_cast<int64_t>(max_dims->batch) * max_dims->hq;
+  const int64_t Hkv = static_cast<int64_t>(max_dims->batch) * max_dims->hkv;
+  const int64_t nb = max_dims->n / kBlk;
+  const int64_t nbw = (nb + 31) / 32;
+  ctx->max_H = H;
+  ctx->max_Hkv = Hkv;
+  ctx->max_nb = nb;
+  ctx->max_nbw = nbw;
+
+  // One allocation, carved into 256-byte aligned pieces.
+  struct Piece {
+    void** p;
+    size_t bytes;
+  };
+  Workspace& w = ctx->ws;
+  w.col_cap = H * nb * (nb + 1) / 2;
+  std::vector<Piece> pieces = {
+      {reinterpret_cast<void**>(&w.st_m), sizeof(float) * H * nb * kBlk},
+      {reinterpret_cast<void**>(&w.st_u), sizeof(float) * H * nb * kBlk},
+      {reinterpret_cast<void**>(&w.st_w), sizeof(float) * H * nb * kBlk},
+      {reinterpret_cast<void**>(&w.anc), sizeof(float) * H * 2 * kBlk},
+      {reinterpret_cast<void**>(&w.rowM), sizeof(float) * H * kBlk},
+      {reinterpret_cast<void**>(&w.rowZ), sizeof(float) * H * kBlk},
+      {reinterpret_cast<void**>(&w.pv), sizeof(float) * H * nb},
+      {reinterpret_cast<void**>(&w.pshi), sizeof(float) * H * nb},
+      {reinterpret_cast<void**>(&w.pslo), sizeof(float) * H * nb},
+      {reinterpret_cast<void**>(&w.ps), sizeof(float) * H * nb},
+      {reinterpret_cast<void**>(&w.cstruct), sizeof(float) * H},
+      {reinterpret_cast<void**>(&w.route), static_cast<size_t>(H)},
+      {reinterpret_cast<void**>(&w.mu), sizeof(float) * H * 2},
+      {reinterpret_cast<void**>(&w.counts), sizeof(int32_t) * H * 4},
+      {reinterpret_cast<void**>(&w.selv), static_cast<size_t>(H * nb)},
+      {reinterpret_cast<void**>(&w.sels), static_cast<size_t>(H * nb)},
+      {reinterpret_cast<void**>(&w.qbar), sizeof(float) * H * nb * kD},
+      {reinterpret_cast<void**>(&w.kbar), sizeof(float) * Hkv * nb * kD},
+      {reinterpret_cast<void**>(&w.pev), sizeof(float) * H * nb * nb},
+      {reinterpret_cast<void**>(&w.hist_cnt), sizeof(unsigned long long) * H * 256},
+      {reinterpret_cast<void**>(&w.hist_mass), sizeof(double) * H * 256},
+      {reinterpret_cast<void**>(&w.pe), sizeof(PeState) * H},
+      {reinterpret_cast<void**>(&w.eq_off), sizeof(int64_t) * H * (nb + 1)},
+      {reinterpret_cast<void**>(&w.rowmask), sizeof(uint32_t) * H * nb * nbw},
+      {reinterpret_cast<void**>(&w.row_cnt), sizeof(int64_t) * H * nb},
+      {reinterpret_cast<void**>(&w.row_ptr), sizeof(int64_t) * (H * nb + 1)},
+      {reinterpret_cast<void**>(&w.col), sizeof(int32_t) * w.col_cap},
+      {reinterpret_cast<void**>(&w.err), sizeof(uint32_t)},
+  };
+  size_t total = 0;
+  for (auto& pc : pieces) total += (pc.bytes + 255) & ~static_cast<size_t>(255);
+  void* base = nullptr;
+  if (cudaMalloc(&base, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete ctx;
+    return CRISP_ERR_NO_MEMORY;
+  }
+  size_t off = 0;
+  for (auto& pc : pieces) {
+    *pc.p = static_cast<char*>(base) + off;
+    off += (pc.bytes + 255) & ~static_cast<size_t>(255);
+  }
+  if (cudaMemset(w.err, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(base);
+    delete ctx;
+    return CRISP_ERR_CUDA;
+  }
+  *out = ctx;
+  return CRISP_OK;
+}
+
+void crisp_destroy(crisp_ctx ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  cudaFree(ctx->ws.st_m);  // the first piece is the allocation's base
+  delete ctx;
+}
+
+crisp_status crisp_select(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                          const crisp_cfg* cfg, void* stream) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if ((st = check_cfg(cfg)) != CRISP_OK) return st;
+  if (!Q || !K || !aligned16(Q) || !aligned16(K)) return CRISP_ERR_INVALID_ARG;
+  const Shape s = make_shape(*dims);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  CUtensorMap tmQ, tmK;
+  if ((st = make_map(ctx, &tmQ, Q, static_cast<int64_t>(s.H) * s.n)) != CRISP_OK) return st;
+  if ((st = make_map(ctx, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
+  ctx->has_sel = false;
+  if ((st = launched(ctx, launch_patsearch(ctx, s, *cfg, tmQ, tmK, cs), "patsearch")) != CRISP_OK)
+    return st;
+  if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, cs), "pe_index")) != CRISP_OK)
+    return st;
+  if ((st = launched(ctx, launch_build_csr(ctx, s, cs), "build_csr")) != CRISP_OK) return st;
+  ctx->has_sel = true;
+  ctx->sel_dims = *dims;
+  return CRISP_OK;
+}
+
+static bool same_dims(const crisp_dims& a, const crisp_dims& b) {
+  return a.batch == b.batch && a.n == b.n && a.hq == b.hq && a.hkv == b.hkv && a.d == b.d;
+}
+
+static crisp_status run_attention(crisp_ctx ctx, const crisp_dims* dims, const void* Q,
+                                  const void* K, const void* V, void* O, bool dense,
+                                  void* stream) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+    return CRISP_ERR_INVALID_ARG;
+  if (!dense && (!ctx->has_sel || !same_dims(ctx->sel_dims, *dims))) return CRISP_ERR_NO_SELECTION;
+  const Shape s = make_shape(*dims);
+  CUtensorMap tmQ, tmK, tmV;
+  if ((st = make_map(ctx, &tmQ, Q, static_cast<int64_t>(s.H) * s.n)) != CRISP_OK) return st;
+  if ((st = make_map(ctx, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
+  if ((st = make_map(ctx, &tmV, V, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
+  return launched(ctx,
+                  launch_attention(ctx, s, tmQ, tmK, tmV, O, dense, static_cast<cudaStream_t>(stream)),
+                  "attention");
+}
+
+crisp_status crisp_attend(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                          const void* V, void* O, void* stream) {
+  return run_attention(ctx, dims, Q, K, V, O, false, stream);
+}
+
+crisp_status crisp_dense(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                         const void* V, void* O, void* stream) {
+  return run_attention(ctx, dims, Q, K, V, O, true, stream);
+}
+
+crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                           const void* V, const crisp_cfg* cfg, void* O, void* stream) {
+  if (!V || !O) return CRISP_ERR_INVALID_ARG;
+  crisp_status st = crisp_select(ctx, dims, Q, K, cfg, stream);
+  if (st != CRISP_OK) return st;
+  return crisp_attend(ctx, dims, Q, K, V, O, stream);
+}
+
+static crisp_status copy_out(crisp_ctx ctx, void* dst, const void* src, size_t bytes) {
+  if (!dst || !bytes) return CRISP_OK;
+  cudaError_t e = cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);
+  return launched(ctx, e, "copy selection");
+}
+
+crisp_status crisp_selection_get(crisp_ctx ctx, const crisp_dims* dims, void* stream,
+                                 crisp_selection_host* out) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if (!out) return CRISP_ERR_INVALID_ARG;
+  if (!ctx->has_sel || !same_dims(ctx->sel_dims, *dims)) return CRISP_ERR_NO_SELECTION;
+  if ((st = launched(ctx, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "sync")) != CRISP_OK)
+    return st;
+  const Shape s = make_shape(*dims);
+  const size_t H = s.H, nb = s.nb, rows = H * nb;
+  const Workspace& w = ctx->ws;
+  if ((st = copy_out(ctx, out->route_vs, w.route, H)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->c_struct, w.cstruct, H * 4)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->mu, w.mu, H * 8)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->counts, w.counts, H * 16)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->p_v, w.pv, H * nb * 4)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->p_s, w.ps, H * nb * 4)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->sel_v, w.selv, H * nb)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, out->sel_s, w.sels, H * nb)) != CRISP_OK) return st;
+  int64_t nnz = 0;
+  if ((st = copy_out(ctx, &nnz, w.row_ptr + rows, sizeof(int64_t))) != CRISP_OK) return st;
+  out->nnz = nnz;
+  if ((st = copy_out(ctx, out->row_ptr, w.row_ptr, (rows + 1) * 8)) != CRISP_OK) return st;
+  if (out->col) {
+    if (out->col_capacity < nnz) return CRISP_ERR_INVALID_ARG;
+    if ((st = copy_out(ctx, out->col, w.col, static_cast<size_t>(nnz) * 4)) != CRISP_OK) return st;
+  }
+  return CRISP_OK;
+}
+
+crisp_status crisp_selection_set(crisp_ctx ctx, const crisp_dims* dims, void* stream,
+                                 const int64_t* row_ptr, const int32_t* col, int64_t nnz) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if (!row_ptr || !col || nnz <= 0) return CRISP_ERR_INVALID_ARG;
+  const Shape s = make_shape(*dims);
+  const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
+  if (row_ptr[0] != 0 || row_ptr[rows] != nnz || nnz > ctx->ws.col_cap) return CRISP_ERR_INVALID_ARG;
+  for (int64_t r = 0; r < rows; ++r) {
+    const int64_t b = row_ptr[r], e = row_ptr[r + 1];
+    if (e <= b) return CRISP_ERR_INVALID_ARG;
+    const int I = static_cast<int>(r % s.nb);
+    for (int64_t k = b; k < e; ++k) {
+      if (col[k] < 0 || col[k] > I) return CRISP_ERR_INVALID_ARG;
+      if (k > b && col[k] <= col[k - 1]) return CRISP_ERR_INVALID_ARG;
+    }
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if ((st = launched(ctx, cudaStreamSynchronize(cs), "sync")) != CRISP_OK) return st;
+  if ((st = launched(ctx, cudaMemcpy(ctx->ws.row_ptr, row_ptr, (rows + 1) * 8, cudaMemcpyHostToDevice),
+                     "upload row_ptr")) != CRISP_OK)
+    return st;
+  if ((st = launched(ctx, cudaMemcpy(ctx->ws.col, col, nnz * 4, cudaMemcpyHostToDevice),
+                     "upload col")) != CRISP_OK)
+    return st;
+  ctx->has_sel = true;
+  ctx->sel_dims = *dims;
+  return CRISP_OK;
+}
+
+crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* stream,
+                                   crisp_stats* out) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if (!out) return CRISP_ERR_INVALID_ARG;
+  if (!ctx->has_sel || !same_dims(ctx->sel_dims, *dims)) return CRISP_ERR_NO_SELECTION;
+  if ((st = launched(ctx, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "sync")) != CRISP_OK)
+    return st;
+  const Shape s = make_shape(*dims);
+  const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
+  std::vector<int64_t> rp(rows + 1);
+  std::vector<uint8_t> route(s.H);
+  std::vector<int32_t> counts(4 * s.H);
+  if ((st = copy_out(ctx, rp.data(), ctx->ws.row_ptr, (rows + 1) * 8)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, route.data(), ctx->ws.route, s.H)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, counts.data(), ctx->ws.counts, 16 * s.H)) != CRISP_OK) return st;
+  out->nnz = rp[rows];
+  out->rows = rows;
+  out->max_row = 0;
+  for (int64_t r = 0; r < rows; ++r)
+    if (rp[r + 1] - rp[r] > out->max_row) out->max_row = rp[r + 1] - rp[r];
+  out->n_vs = 0;
+  out->n_pe = 0;
+  out->pe_rescued = 0;
+  for (int h = 0; h < s.H; ++h) {
+    if (route[h]) {
+      ++out->n_vs;
+    } else {
+      ++out->n_pe;
+      out->pe_rescued += counts[4 * h + 1];
+    }
+  }
+  return CRISP_OK;
+}
+
+crisp_status crisp_sync_status(crisp_ctx ctx, void* stream) {
+  if (!ctx) return CRISP_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_err(ctx, "stream", e);
+    return CRISP_ERR_CUDA;
+  }
+  uint32_t word = 0;
+  if ((e = cudaMemcpy(&word, ctx->ws.err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess) {
+    set_err(ctx, "read error word", e);
+    return CRISP_ERR_CUDA;
+  }
+  if (word) cudaMemset(ctx->ws.err, 0, 4);
+  if (word & kErrTimeout) return CRISP_ERR_TIMEOUT;
+  if (word & kErrRange) return CRISP_ERR_DEVICE_ASSERT;
+  return CRISP_OK;
+}
+
+crisp_status crisp_set_debug(crisp_ctx ctx, uint32_t flags, uint64_t timeout_ns) {
+  if (!ctx) return CRISP_ERR_INVALID_ARG;
+  ctx->debug_flags = flags;
+  ctx->timeout_ns = timeout_ns ? timeout_ns : 1000000000ull;
+  return CRISP_OK;
+}
+
+const char* crisp_last_error(crisp_ctx ctx) { return ctx ? ctx->last_err : ""; }
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// internal.h -- context layout and kernel launchers shared by the library's translation
+// units.  Not part of the public ABI (include/crisp.h is).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "crisp.h"
+
+namespace crisp {
+
+constexpr int kD = 128;        // head dimension
+constexpr int kBlk = 128;      // block size B = proxy rows b
+constexpr int kTileBytes = kBlk * kD * 2;  // one 128 x 128 bf16 tile
+
+// Radix-select state of one PE head's gamma cut (device).
+struct PeState {
+  uint32_t prefix;          // decided high bits of the threshold
+  uint32_t decided;         // mask of decided bits
+  double mass_above;        // mass of items strictly above the decided range
+  uint32_t thresh;          // threshold bit pattern (after the last pass)
+  uint32_t select_all;      // 1: the whole triangle is taken
+  unsigned long long need_eq;   // items equal to thresh to take, in flat order
+  unsigned long long count_eq;  // items equal to thresh
+};
+
+struct Workspace {
+  // PatSearch per-tile statistics, [H][nb][128] each (log2 domain max, sums under it)
+  float* st_m = nullptr;
+  float* st_u = nullptr;   // keys on or left of the row's diagonal offset (slash block N_b-1-t)
+  float* st_w = nullptr;   // keys right of it (slash block N_b-2-t)
+  float* anc = nullptr;    // [H][2][128] anchor partial sums (tile 0, tile N_b-1)
+  float* rowM = nullptr;   // [H][128]
+  float* rowZ = nullptr;   // [H][128]
+  float* pv = nullptr;     // [H][nb] pooled vertical score
+  float* pshi = nullptr;   // [H][nb] slash contribution of tile t to block N_b-1-t
+  float* pslo = nullptr;   // [H][nb] slash contribution of tile t to block N_b-2-t
+  float* ps = nullptr;     // [H][nb] pooled slash score
+  float* cstruct = nullptr;  // [H]
+  uint8_t* route = nullptr;  // [H] 1 = VS
+  float* mu = nullptr;       // [H][2]
+  int32_t* counts = nullptr; // [H][4]
+  uint8_t* selv = nullptr;   // [H][nb]
+  uint8_t* sels = nullptr;   // [H][nb]
+  // PEIndex
+  float* qbar = nullptr;     // [H][nb][128]
+  float* kbar = nullptr;     // [Hkv][nb][128]
+  float* pev = nullptr;      // [H][nb][nb] pooled logits, then v = A_bar / N_b
+  unsigned long long* hist_cnt = nullptr;  // [H][256]
+  double* hist_mass = nullptr;             // [H][256]
+  PeState* pe = nullptr;                   // [H]
+  int64_t* eq_off = nullptr;               // [H][nb+1]
+  // per-row block masks and CSR
+  uint32_t* rowmask = nullptr;  // [H][nb][nbw]
+  int64_t* row_cnt = nullptr;   // [H*nb]
+  int64_t* row_ptr = nullptr;   // [H*nb+1]
+  int32_t* col = nullptr;       // [col_cap]
+  int64_t col_cap = 0;
+  uint32_t* err = nullptr;      // device error word
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Shapes of one call, flattened: H = batch*hq query heads, Hkv = batch*hkv.
+struct Shape {
+  int n, nb, nbw, H, Hkv, hq, hkv, group;
+};
+
+}  // namespace crisp
+
+struct crisp_ctx_s {
+  int device = 0;
+  int num_sms = 0;
+  crisp_dims maxd{};
+  int64_t max_H = 0, max_Hkv = 0, max_nb = 0, max_nbw = 0;
+  crisp::Workspace ws;
+  crisp::EncodeTiledFn encode = nullptr;
+  bool has_sel = false;
+  crisp_dims sel_dims{};
+  uint32_t debug_flags = 0;
+  uint64_t timeout_ns = 1000000000ull;
+  char last_err[256] = {0};
+};
+
+namespace crisp {
+
+Shape make_shape(const crisp_dims& d);
+
+// Each launcher only enqueues work on `st` and returns the launch status.
+cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
+                             const CUtensorMap& tmQ, const CUtensorMap& tmK, cudaStream_t st);
+cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
+                            const void* K, cudaStream_t st);
+cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st);
+cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& tmQ,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, void* O, bool dense,
+                             cudaStream_t st);
+cudaError_t init_kernel_attributes();
+
+}  // namespace crisp

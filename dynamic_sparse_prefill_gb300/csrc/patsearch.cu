@@ -1,0 +1,538 @@
+// patsearch.cu -- PatSearch proxy attention, C_struct routing and VS index selection.
+//
+// CRISP ("CRISP: Cliff-awaRe Input-adaptive Sparse Prefilling with Structural-Mass-
+// Motivated Routing", paper.rainbus.top), "Core method" step 1 and "Method step details"
+// steps 1-2; Algorithms 2 (PatSearch) and 3 (VSIndex) under "Figures and tables".
+//
+// Per query head: A_hat = causal Softmax(Q[-b:] K^T / sqrt(d)) (b = 128 rows),
+// a_v = column mean, a_s = diagonal mean (delta = query - key position), both pooled by
+// blocks of B = 128, C_struct = anchor mass of a_v, VS iff C_struct >= tau.
+//
+// A_hat is never materialised.  One pass over K (tcgen05 MMA, S in TMEM) records, for
+// every proxy row r and key tile t, the tile's row maximum m and two partial sums of
+// exp2(s - m): u over keys on or left of the row's diagonal offset, w over the others.
+// Because delta = 128*(N_b-1-t) + (r - c) for key column c of tile t, u is exactly the
+// row's mass on slash block N_b-1-t and w its mass on slash block N_b-2-t, and u + w its
+// mass on vertical block t.  A second, cheap kernel rescales the partials with the
+// row's global max and sum, which gives the pooled p_v and p_s directly.
+#include <cfloat>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace crisp {
+
+namespace {
+
+constexpr int kProxyThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kProxyStages = 4;
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+constexpr size_t kProxySmem = 1024 + kTileBytes * (1 + kProxyStages) + 256;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Warp-uniform bounded wait: lane 0 waits, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort, uint64_t tmo) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, abort, tmo) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Wait for asynchronous work this thread issued, ignoring the abort flag (bounded).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                           uint64_t tmo) {
+  volatile int never = 0;
+  mbar_wait(bar, parity, err, &never, tmo);
+}
+
+struct ProxyArgs {
+  int n, nb, hq, hkv, group;
+  int w_sink, w_local;
+  int tiles_per_cta;
+  float scale_log2;
+  float* st_m;
+  float* st_u;
+  float* st_w;
+  float* anc;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(kProxyThreads, 1)
+    proxy_tile_stats_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmK, const ProxyArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sK + kProxyStages * kTileBytes);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + kProxyStages;
+  uint64_t* s_full = k_empty + kProxyStages;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* drain = s_free + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x;  // flattened query head
+  const int t_begin = blockIdx.y * a.tiles_per_cta;
+  const int t_end = min(a.nb, t_begin + a.tiles_per_cta);
+  const int ntiles = t_end - t_begin;
+  if (ntiles <= 0) return;
+  const int hk = (h / a.hq) * a.hkv + (h % a.hq) / a.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kProxyStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      const int qrow = h * a.n + a.n - kBlk;
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      tma_load_2d(sQ, &tmQ, q_full, 0, qrow);
+      tma_load_2d(sQ + kTileBytes / 2, &tmQ, q_full, 64, qrow);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % kProxyStages;
+        if (i >= kProxyStages &&
+            !mbar_wait(&k_empty[s], ((i / kProxyStages) + 1) & 1, a.err, abort_flag, tmo))
+          break;
+        const int krow = hk * a.n + (t_begin + i) * kBlk;
+        uint8_t* dst = sK + s * kTileBytes;
+        mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+        tma_load_2d(dst, &tmK, &k_full[s], 0, krow);
+        tma_load_2d(dst + kTileBytes / 2, &tmK, &k_full[s], 64, krow);
+        ++issued;
+      }
+      drain_wait(q_full, 0, a.err, tmo);
+      for (int i = max(0, issued - kProxyStages); i < issued; ++i)
+        drain_wait(&k_full[i % kProxyStages], (i / kProxyStages) & 1, a.err, tmo);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (mbar_wait(q_full, 0, a.err, abort_flag, tmo)) {
+        const uint32_t q_base = smem_u32(sQ);
+        for (int i = 0; i < ntiles; ++i) {
+          const int s = i % kProxyStages, sb = i & 1;
+          if (!mbar_wait(&k_full[s], (i / kProxyStages) & 1, a.err, abort_flag, tmo)) break;
+          if (i >= 2 && !mbar_wait(&s_free[sb], ((i >> 1) + 1) & 1, a.err, abort_flag, tmo))
+            break;
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(sK + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+            umma_bf16(tmem + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
+                      sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[sb]);
+          umma_commit(&k_empty[s]);
+        }
+      }
+      umma_commit(drain);
+      drain_wait(drain, 0, a.err, tmo);
+    }
+  } else {
+    // Epilogue: thread <-> proxy row r (TMEM lane), 4 warps cover the 4 lane quarters.
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t row_taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    for (int i = 0; i < ntiles; ++i) {
+      const int sb = i & 1;
+      if (!warp_wait(&s_full[sb], (i >> 1) & 1, a.err, abort_flag, tmo)) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(row_taddr + sb * 128 + c * 32, v[c]);
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
+
+      const int t = t_begin + i;
+      const bool last = (t == a.nb - 1);
+      const int j0 = t * kBlk;
+      float mx = -FLT_MAX;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int col = c4 * 32 + c;
+          const float s2 = __uint_as_float(v[c4][c]) * a.scale_log2;
+          if (!last || col <= r) mx = fmaxf(mx, s2);
+        }
+      float u = 0.f, w = 0.f, an = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int col = c4 * 32 + c;
+          const float s2 = __uint_as_float(v[c4][c]) * a.scale_log2;
+          const bool valid = !last || col <= r;
+          const float e = valid ? fast_exp2(s2 - mx) : 0.f;
+          if (col <= r)
+            u += e;
+          else
+            w += e;
+          const int j = j0 + col;
+          const bool anchor = (t == 0 && j < a.w_sink) || (last && j >= a.n - a.w_local);
+          if (anchor) an += e;
+        }
+      const size_t idx = (static_cast<size_t>(h) * a.nb + t) * kBlk + r;
+      a.st_m[idx] = mx;
+      a.st_u[idx] = u;
+      a.st_w[idx] = w;
+      if (t == 0) {
+        a.anc[(static_cast<size_t>(h) * 2 + 0) * kBlk + r] = an;
+        if (last) a.anc[(static_cast<size_t>(h) * 2 + 1) * kBlk + r] = 0.f;
+      } else if (last) {
+        a.anc[(static_cast<size_t>(h) * 2 + 1) * kBlk + r] = an;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// Row maximum M_r and normaliser Z_r of every proxy row over all key tiles.
+__global__ void __launch_bounds__(1024) proxy_row_stats_kernel(const float* __restrict__ st_m,
+                                                               const float* __restrict__ st_u,
+                                                               const float* __restrict__ st_w,
+                                                               int nb, float* rowM,
+                                                               float* rowZ) {
+  __shared__ float sM[8][kBlk], sZ[8][kBlk];
+  const int h = blockIdx.x;
+  const int r = threadIdx.x & 127, slice = threadIdx.x >> 7;
+  float M = -FLT_MAX, Z = 0.f;
+  for (int t = slice; t < nb; t += 8) {
+    const size_t idx = (static_cast<size_t>(h) * nb + t) * kBlk + r;
+    const float m = st_m[idx];
+    const float s = st_u[idx] + st_w[idx];
+    if (m > M) {
+      Z = Z * fast_exp2(M - m) + s;
+      M = m;
+    } else {
+      Z += s * fast_exp2(m - M);
+    }
+  }
+  sM[slice][r] = M;
+  sZ[slice][r] = Z;
+  __syncthreads();
+  if (slice == 0) {
+    float Mt = -FLT_MAX;
+    for (int i = 0; i < 8; ++i) Mt = fmaxf(Mt, sM[i][r]);
+    float Zt = 0.f;
+    for (int i = 0; i < 8; ++i) Zt += sZ[i][r] * fast_exp2(sM[i][r] - Mt);
+    rowM[h * kBlk + r] = Mt;
+    rowZ[h * kBlk + r] = Zt;
+  }
+}
+
+// Pooled vertical and slash contributions of every key tile: a warp per tile.
+__global__ void __launch_bounds__(256) proxy_pool_kernel(
+    const float* __restrict__ st_m, const float* __restrict__ st_u,
+    const float* __restrict__ st_w, const float* __restrict__ rowM,
+    const float* __restrict__ rowZ, int nb, float inv_b, float* pv, float* pshi, float* pslo) {
+  __shared__ float sM[kBlk], sIZ[kBlk];
+  const int h = blockIdx.y;
+  if (threadIdx.x < kBlk) {
+    sM[threadIdx.x] = rowM[h * kBlk + threadIdx.x];
+    sIZ[threadIdx.x] = 1.f / rowZ[h * kBlk + threadIdx.x];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= nb) return;
+  float su = 0.f, sw = 0.f;
+  const size_t base = (static_cast<size_t>(h) * nb + t) * kBlk;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = lane + 32 * k;
+    const float e = fast_exp2(st_m[base + r] - sM[r]) * sIZ[r];
+    su += st_u[base + r] * e;
+    sw += st_w[base + r] * e;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    su += __shfl_xor_sync(0xffffffffu, su, o);
+    sw += __shfl_xor_sync(0xffffffffu, sw, o);
+  }
+  if (lane == 0) {
+    pv[static_cast<size_t>(h) * nb + t] = (su + sw) * inv_b;
+    pshi[static_cast<size_t>(h) * nb + t] = su * inv_b;
+    pslo[static_cast<size_t>(h) * nb + t] = sw * inv_b;
+  }
+}
+
+struct RouteArgs {
+  int nb;
+  float inv_b, tau, alpha;
+  int kmin_blocks;
+  uint32_t flags;
+  const float* st_m;
+  const float* anc;
+  const float* rowM;
+  const float* rowZ;
+  const float* pv;
+  const float* pshi;
+  const float* pslo;
+  float* ps;
+  float* cstruct;
+  uint8_t* route;
+  float* mu;
+  int32_t* counts;
+  uint8_t* selv;
+  uint8_t* sels;
+};
+
+__device__ float block_sum_1024(float x, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  float t = lane < (blockDim.x >> 5) ? red[lane] : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+__device__ int block_count_1024(int x, int* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  int t = lane < (blockDim.x >> 5) ? red[lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+// Larger value wins; equal values go to the lower index.
+__device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// Blocks with p > thr, then (if fewer than kmin) the largest remaining ones until
+// k = clip(count, kmin, nb) are kept.  Returns count and k.
+__device__ void select_direction(const float* p, uint8_t* sel, int nb, float thr, int kmin,
+                                 int* red, float* redf, int* out_c, int* out_k) {
+  int local = 0;
+  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+    const uint8_t s = p[J] > thr ? 1 : 0;
+    sel[J] = s;
+    local += s;
+  }
+  const int c = block_count_1024(local, red);
+  const int k = min(max(c, kmin), nb);
+  for (int it = c; it < k; ++it) {
+    float bv = -1.f;
+    int bi = 0x7fffffff;
+    for (int J = threadIdx.x; J < nb; J += blockDim.x)
+      if (!sel[J]) better(bv, bi, p[J], J);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      better(bv, bi, v2, i2);
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+      redf[threadIdx.x >> 5] = bv;
+      red[threadIdx.x >> 5] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float fv = redf[0];
+      int fi = red[0];
+      for (int wi = 1; wi < (int)(blockDim.x >> 5); ++wi) better(fv, fi, redf[wi], red[wi]);
+      if (fi >= 0 && fi < nb) sel[fi] = 1;
+    }
+    __syncthreads();
+  }
+  *out_c = c;
+  *out_k = k;
+}
+
+__global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a) {
+  extern __shared__ float sdyn[];
+  float* spv = sdyn;
+  float* sps = sdyn + a.nb;
+  uint8_t* ssv = reinterpret_cast<uint8_t*>(sps + a.nb);
+  uint8_t* sss = ssv + a.nb;
+  __shared__ int red[32];
+  __shared__ float redf[32];
+  const int h = blockIdx.x;
+  const int nb = a.nb;
+  const size_t hb = static_cast<size_t>(h) * nb;
+
+  // C_struct = (1/b) sum_r (anchor mass of row r) -- "Core method" step 1, Algorithm 2.
+  float c = 0.f;
+  if (threadIdx.x < kBlk) {
+    const int r = threadIdx.x;
+    const float M = a.rowM[h * kBlk + r];
+    const float iz = 1.f / a.rowZ[h * kBlk + r];
+    c = a.anc[(static_cast<size_t>(h) * 2) * kBlk + r] *
+        fast_exp2(a.st_m[hb * kBlk + r] - M);
+    if (nb > 1)
+      c += a.anc[(static_cast<size_t>(h) * 2 + 1) * kBlk + r] *
+           fast_exp2(a.st_m[(hb + nb - 1) * kBlk + r] - M);
+    c *= iz;
+  }
+  const float C = block_sum_1024(c, redf) * a.inv_b;
+  bool vs = C >= a.tau;
+  if (a.flags & CRISP_FLAG_FORCE_VS) vs = true;
+  if (a.flags & CRISP_FLAG_FORCE_PE) vs = false;
+
+  // p_v[J] = tile J's vertical mass; p_s[J] = hi part of tile N_b-1-J + lo part of N_b-2-J.
+  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+    spv[J] = a.pv[hb + J];
+    float s = a.pshi[hb + (nb - 1 - J)];
+    if (J <= nb - 2) s += a.pslo[hb + (nb - 2 - J)];
+    sps[J] = s;
+    a.ps[hb + J] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a.cstruct[h] = C;
+    a.route[h] = vs ? 1 : 0;
+    for (int i = 0; i < 4; ++i) a.counts[h * 4 + i] = 0;
+  }
+  if (!vs) {
+    for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+      a.selv[hb + J] = 0;
+      a.sels[hb + J] = 0;
+    }
+    if (threadIdx.x == 0) {
+      a.mu[h * 2] = 0.f;
+      a.mu[h * 2 + 1] = 0.f;
+    }
+    return;
+  }
+  // Noise floor mu_d = max(1 - p_d[0] - p_d[N_b-1], 0)/(N_b-2)  (Algorithm 3).
+  const float mu_v = nb > 2 ? fmaxf(1.f - spv[0] - spv[nb - 1], 0.f) / (nb - 2) : 0.f;
+  const float mu_s = nb > 2 ? fmaxf(1.f - sps[0] - sps[nb - 1], 0.f) / (nb - 2) : 0.f;
+  int cv, kv, cs, ks;
+  select_direction(spv, ssv, nb, a.alpha * mu_v, a.kmin_blocks, red, redf, &cv, &kv);
+  __syncthreads();
+  select_direction(sps, sss, nb, a.alpha * mu_s, a.kmin_blocks, red, redf, &cs, &ks);
+  __syncthreads();
+  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+    a.selv[hb + J] = ssv[J];
+    a.sels[hb + J] = sss[J];
+  }
+  if (threadIdx.x == 0) {
+    a.mu[h * 2] = mu_v;
+    a.mu[h * 2 + 1] = mu_s;
+    a.counts[h * 4 + 0] = cv;
+    a.counts[h * 4 + 1] = cs;
+    a.counts[h * 4 + 2] = kv;
+    a.counts[h * 4 + 3] = ks;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
+                             const CUtensorMap& tmQ, const CUtensorMap& tmK, cudaStream_t st) {
+  Workspace& w = ctx->ws;
+  ProxyArgs a;
+  a.n = s.n;
+  a.nb = s.nb;
+  a.hq = s.hq;
+  a.hkv = s.hkv;
+  a.group = s.group;
+  a.w_sink = cfg.w_sink;
+  a.w_local = cfg.w_local;
+  // about three waves of CTAs over (head, tile chunk)
+  const int want = max(1, (3 * ctx->num_sms + s.H - 1) / s.H);
+  const int chunks = min(s.nb, want);
+  a.tiles_per_cta = (s.nb + chunks - 1) / chunks;
+  const int nchunks = (s.nb + a.tiles_per_cta - 1) / a.tiles_per_cta;
+  a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
+  a.st_m = w.st_m;
+  a.st_u = w.st_u;
+  a.st_w = w.st_w;
+  a.anc = w.anc;
+  a.err = w.err;
+  a.timeout_ns = ctx->timeout_ns;
+  proxy_tile_stats_kernel<<<dim3(s.H, nchunks), kProxyThreads, kProxySmem, st>>>(tmQ, tmK, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  proxy_row_stats_kernel<<<s.H, 1024, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb, w.rowM, w.rowZ);
+  proxy_pool_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(
+      w.st_m, w.st_u, w.st_w, w.rowM, w.rowZ, s.nb, 1.f / kBlk, w.pv, w.pshi, w.pslo);
+  RouteArgs r;
+  r.nb = s.nb;
+  r.inv_b = 1.f / kBlk;
+  r.tau = cfg.tau_proxy;
+  r.alpha = cfg.alpha;
+  r.kmin_blocks = (cfg.k_min_tokens + kBlk - 1) / kBlk;
+  r.flags = cfg.flags;
+  r.st_m = w.st_m;
+  r.anc = w.anc;
+  r.rowM = w.rowM;
+  r.rowZ = w.rowZ;
+  r.pv = w.pv;
+  r.pshi = w.pshi;
+  r.pslo = w.pslo;
+  r.ps = w.ps;
+  r.cstruct = w.cstruct;
+  r.route = w.route;
+  r.mu = w.mu;
+  r.counts = w.counts;
+  r.selv = w.selv;
+  r.sels = w.sels;
+  const size_t dyn = static_cast<size_t>(s.nb) * (2 * sizeof(float) + 2);
+  route_vs_select_kernel<<<s.H, 1024, dyn, st>>>(r);
+  return cudaGetLastError();
+}
+
+cudaError_t init_patsearch_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(proxy_tile_stats_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kProxySmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(route_vs_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              1 << 17);
+}
+
+}  // namespace crisp

@@ -1,0 +1,178 @@
+/*
+ * crisp.h -- C ABI of the GB300 (sm_103a) CRISP sparse-prefill attention library.
+ *
+ * CRISP is described on the analysis page "CRISP: Cliff-awaRe Input-adaptive Sparse
+ * Prefilling with Structural-Mass-Motivated Routing" (paper.rainbus.top/paper/2609.01925).
+ * Section names below are that page's:
+ *   "Method step details"  -- Algorithm 1: PatSearch -> VSIndex | PEIndex -> A(Q,K,V,S),
+ *                             with tau_proxy=0.2, gamma=0.95, alpha in {1.0,1.25}, B=128,
+ *                             k_min=1024 tokens per direction.
+ *   "Core method"          -- step 1 PatSearch and C_struct routing; the noise floor.
+ *   "Prerequisites"        -- A(Q,K,V,S) = Softmax(QK^T/sqrt(d) + M_S) V.
+ *   "Figures and tables"   -- descriptions of Algorithms 2 (PatSearch), 3 (VSIndex) and
+ *                             4 (PEIndex).
+ *
+ * Conventions for every entry point:
+ *   - Q is [batch, hq, n, d], K and V are [batch, hkv, n, d], O is [batch, hq, n, d]; all
+ *     bf16, contiguous, head-major, in device memory owned by the caller.  Query head h
+ *     uses key/value head h / (hq/hkv) of the same batch entry (GQA).
+ *   - Supported shapes: d == 128, n a multiple of 128 with 128 <= n <= 1048576,
+ *     hq % hkv == 0, batch*hq <= 65535.  Parameters: B == b == 128,
+ *     1 <= w_sink, w_local <= 128, 0 < gamma <= 1, alpha >= 0, k_min_tokens >= 0.
+ *     Anything else returns CRISP_ERR_INVALID_ARG or CRISP_ERR_UNSUPPORTED before any
+ *     work is queued.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute entry points
+ *     only enqueue work on it and return; they never synchronise.  The *_get, *_set,
+ *     *_stats and crisp_sync_status calls synchronise `stream`.
+ *   - The context owns every device buffer the path needs (allocated once by
+ *     crisp_create for the largest dims it will see) and the current selection.  A
+ *     context must not be used from two host threads at once, and work queued with one
+ *     context must not overlap on two streams.
+ *   - No call aborts, traps or throws.  Argument errors come back synchronously.  Errors
+ *     met on the device (a bounded wait that ran out, an index out of range) are latched
+ *     in a device error word and reported by the next crisp_sync_status.
+ */
+#ifndef CRISP_H
+#define CRISP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CRISP_OK = 0,
+  CRISP_ERR_INVALID_ARG = 1,   /* null pointer, bad shape or parameter             */
+  CRISP_ERR_UNSUPPORTED = 2,   /* valid but not implemented (d != 128, B != 128...) */
+  CRISP_ERR_NO_MEMORY = 3,     /* device allocation failed                          */
+  CRISP_ERR_CUDA = 4,          /* a CUDA runtime call failed (see crisp_last_error)  */
+  CRISP_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out                    */
+  CRISP_ERR_DEVICE_ASSERT = 6, /* a kernel's range check failed                      */
+  CRISP_ERR_NO_SELECTION = 7   /* crisp_attend / *_get before any selection exists  */
+} crisp_status;
+
+typedef struct {
+  int32_t batch; /* batch entries                        */
+  int32_t n;     /* tokens per sequence                  */
+  int32_t hq;    /* query heads                          */
+  int32_t hkv;   /* key/value heads                      */
+  int32_t d;     /* head dimension (128)                 */
+} crisp_dims;
+
+/* Method parameters ("Method step details"). */
+typedef struct {
+  int32_t B;            /* key/query block size (128)                                 */
+  int32_t b;            /* proxy queries: the last b rows of Q (128)                   */
+  int32_t w_sink;       /* anchor: first w_sink keys (128)                             */
+  int32_t w_local;      /* anchor: last w_local keys (128)                             */
+  int32_t k_min_tokens; /* minimum VS budget per direction, tokens (1024 = 8 blocks)   */
+  float tau_proxy;      /* route VS iff C_struct >= tau_proxy (0.2)                    */
+  float alpha;          /* VS: keep blocks with p_d > alpha * mu_d (1.0)               */
+  float gamma;          /* PE: cumulative coverage target (0.95)                      */
+  uint32_t flags;       /* CRISP_FLAG_*                                                */
+} crisp_cfg;
+
+#define CRISP_FLAG_FORCE_VS 0x1u /* route every head VS (C_struct still computed) */
+#define CRISP_FLAG_FORCE_PE 0x2u /* route every head PE                          */
+
+/* Debug flags for crisp_set_debug. */
+#define CRISP_DEBUG_DROP_ARRIVE 0x1u /* attention: skip one barrier arrive in the first
+                                        work item so a bounded wait runs out (tests the
+                                        timeout path; the kernel still exits cleanly)   */
+
+typedef struct crisp_ctx_s* crisp_ctx;
+
+/* The page's defaults: B=b=128, w_sink=w_local=128, k_min=1024, tau=0.2, alpha=1, gamma=0.95. */
+crisp_cfg crisp_cfg_default(void);
+
+/* Allocate a context and all device workspace for problems up to `max_dims` on the
+ * current CUDA device.  Returns CRISP_ERR_NO_MEMORY if the workspace does not fit. */
+crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out);
+
+/* Free the context and its workspace (synchronises the device first). NULL is a no-op. */
+void crisp_destroy(crisp_ctx ctx);
+
+/* Steps 1-3 of Algorithm 1 ("Method step details"; Algorithms 2, 3, 4 under "Figures and
+ * tables"): per query head, the proxy attention of the last b queries, C_struct and the
+ * VS/PE route; then the VS sink-aware noise-floor selection or the PE pooled
+ * gamma-cumsum selection; then the per-query-block key-block lists (CSR, sorted).
+ * Reads Q and K; writes only context buffers.  The selection stays in the context. */
+crisp_status crisp_select(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                          const crisp_cfg* cfg, void* stream);
+
+/* Step 4 ("Method step details"; "Prerequisites" A(Q,K,V,S)): exact causal softmax
+ * attention of every query block over its selected key blocks (token-causal inside the
+ * diagonal block), using the context's current selection (from crisp_select or
+ * crisp_selection_set with the same dims).  Writes O. */
+crisp_status crisp_attend(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                          const void* V, void* O, void* stream);
+
+/* crisp_select followed by crisp_attend: CRISP(Q,K,V) -> O (Algorithm 1). */
+crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                           const void* V, const crisp_cfg* cfg, void* O, void* stream);
+
+/* Dense causal attention with the same kernel and every key block K <= I: the in-library
+ * denominator of the speedup ("Prerequisites", FlashAttention).  Writes O; does not touch
+ * the selection. */
+crisp_status crisp_dense(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                         const void* V, void* O, void* stream);
+
+/* Host copy of the current selection.  Every pointer is caller-owned host memory and may
+ * be NULL to skip that field.  H = batch*hq, N_b = n/128. */
+typedef struct {
+  uint8_t* route_vs;    /* [H]        1 = VS, 0 = PE                                  */
+  float* c_struct;      /* [H]        C_struct                                       */
+  float* mu;            /* [H][2]     mu_v, mu_s (VS heads; 0 for PE)                 */
+  int32_t* counts;      /* [H][4]     VS: c_v, c_s, k_v, k_s.
+                                      PE: pairs kept by the gamma cut, rescued rows, 0, 0 */
+  float* p_v;           /* [H][N_b]   pooled vertical score (all heads)               */
+  float* p_s;           /* [H][N_b]   pooled slash score (all heads)                  */
+  uint8_t* sel_v;       /* [H][N_b]   S_v membership (VS heads)                        */
+  uint8_t* sel_s;       /* [H][N_b]   S_s membership (VS heads)                        */
+  int64_t* row_ptr;     /* [H*N_b+1]  CSR row offsets, row = h*N_b + I                 */
+  int32_t* col;         /* [col_capacity] key blocks, ascending within a row           */
+  int64_t col_capacity; /* in: size of `col` (entries)                                 */
+  int64_t nnz;          /* out: number of selected (query block, key block) pairs      */
+} crisp_selection_host;
+
+crisp_status crisp_selection_get(crisp_ctx ctx, const crisp_dims* dims, void* stream,
+                                 crisp_selection_host* out);
+
+/* Replace the context's selection by a caller-supplied CSR (host arrays, H*N_b+1 row
+ * offsets and nnz key blocks).  Each row must be strictly ascending with entries in
+ * [0, I]; rows must be non-empty.  Checked on the host: CRISP_ERR_INVALID_ARG otherwise. */
+crisp_status crisp_selection_set(crisp_ctx ctx, const crisp_dims* dims, void* stream,
+                                 const int64_t* row_ptr, const int32_t* col, int64_t nnz);
+
+typedef struct {
+  int64_t nnz;         /* selected block pairs over all heads                          */
+  int64_t rows;        /* query-block rows (H*N_b)                                      */
+  int64_t max_row;     /* longest row                                                    */
+  int64_t pe_rescued;  /* PE rows whose only block is the forced diagonal               */
+  int32_t n_vs;        /* heads routed VS                                                */
+  int32_t n_pe;        /* heads routed PE                                                */
+} crisp_stats;
+
+crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* stream,
+                                   crisp_stats* out);
+
+/* Synchronise `stream`, then report and clear the device error word: CRISP_OK,
+ * CRISP_ERR_TIMEOUT or CRISP_ERR_DEVICE_ASSERT, or CRISP_ERR_CUDA if the stream itself
+ * reports a CUDA error. */
+crisp_status crisp_sync_status(crisp_ctx ctx, void* stream);
+
+/* Debug controls: CRISP_DEBUG_* flags and the bounded-wait limit in nanoseconds
+ * (0 = default, one second). */
+crisp_status crisp_set_debug(crisp_ctx ctx, uint32_t flags, uint64_t timeout_ns);
+
+const char* crisp_status_string(crisp_status s);
+
+/* Text of the last CUDA error seen by this context ("" if none). */
+const char* crisp_last_error(crisp_ctx ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CRISP_H */

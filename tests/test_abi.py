@@ -1,0 +1,71 @@
+"""CPU checks of the C ABI: the library loads, exports every function include/crisp.h
+declares, and validates arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from dynamic_sparse_prefill_gb300 import _lib
+    return _lib
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "crisp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(crisp_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    lib = L.lib()
+    decl = declared_functions()
+    assert decl == sorted(L.EXPORTED)
+    for name in decl:
+        assert hasattr(lib, name), name
+
+
+def test_default_cfg_is_the_pages_defaults(L):
+    c = L.lib().crisp_cfg_default()
+    assert (c.B, c.b, c.w_sink, c.w_local, c.k_min_tokens) == (128, 128, 128, 128, 1024)
+    assert abs(c.tau_proxy - 0.2) < 1e-7 and c.alpha == 1.0 and abs(c.gamma - 0.95) < 1e-7
+    assert c.flags == 0
+
+
+def test_status_strings(L):
+    lib = L.lib()
+    for s in range(8):
+        assert lib.crisp_status_string(s)
+    assert lib.crisp_status_string(5) == b"device wait timed out"
+
+
+@pytest.mark.parametrize("dims,status", [
+    ((1, 4096, 2, 2, 64), 2),     # d != 128
+    ((1, 4000, 2, 2, 128), 2),    # n not a multiple of 128
+    ((1, 0, 2, 2, 128), 1),
+    ((1, 4096, 3, 2, 128), 1),    # hq % hkv != 0
+    ((0, 4096, 2, 2, 128), 1),
+    ((1, 1 << 21, 2, 2, 128), 2),  # beyond the supported length
+])
+def test_create_rejects_bad_dims_on_host(L, dims, status):
+    lib = L.lib()
+    h = ctypes.c_void_p()
+    d = L.Dims(*dims)
+    assert lib.crisp_create(ctypes.byref(d), ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_null_arguments(L):
+    lib = L.lib()
+    assert lib.crisp_create(None, None) == 1
+    d = L.Dims(1, 4096, 2, 2, 128)
+    assert lib.crisp_select(None, ctypes.byref(d), None, None, None, None) == 1
+    assert lib.crisp_sync_status(None, None) == 1
+    lib.crisp_destroy(None)
+    assert lib.crisp_last_error(None) == b""

@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Every workload is seeded and synthetic (workloads/).  Selections (routes, VS block sets,
+PE pair sets, CSR rows) must be bit-exact up to counted near-threshold items; outputs on
+the oracle's own index set must be within max abs 2e-2 / mean abs 2e-3 (tests/parity.py).
+"""
+import numpy as np
+import pytest
+
+from tests.parity import (compare_outputs, compare_selection, csr_from_masks, oracle_outputs,
+                          oracle_select, to_device)
+from workloads import get
+from workloads.configs import Workload
+from workloads.planted import generate, random_qkv
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dsp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dynamic_sparse_prefill_gb300 as d
+    return d
+
+
+def _cfg(dsp, w, **kw):
+    return dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy,
+                           k_min_tokens=w.k_min_tokens, w_sink=w.w_sink, w_local=w.w_local,
+                           **kw)
+
+
+def _rows(blocks, B=128):
+    return np.concatenate([np.arange(I * B, (I + 1) * B) for I in blocks])
+
+
+def run_parity(dsp, w, g, sample=None, seed=0, flags=0, report=None):
+    """Full selection parity, then output parity on the oracle's index set.
+
+    sample: None for every query block of every head, else (n_heads, n_blocks) drawn
+    with `seed`.
+    """
+    nb = w.n_blocks
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    cfg = _cfg(dsp, w, flags=flags)
+    o = torch.empty_like(q)
+    ctx.prefill(dims, q, k, v, cfg, o)
+    assert ctx.sync_status() == 0
+    sel = ctx.selection_get(dims)
+    force = None
+    if flags & dsp.FLAG_FORCE_VS:
+        force = "vs"
+    if flags & dsp.FLAG_FORCE_PE:
+        force = "pe"
+    osel = oracle_select(w, g) if force is None else _oracle_forced(w, g, force)
+    rep = compare_selection(w, sel, osel)
+
+    if sample is None:
+        blocks = {h: list(range(nb)) for h in range(w.hq)}
+    else:
+        rng = np.random.default_rng(seed)
+        hs = rng.choice(w.hq, size=min(sample[0], w.hq), replace=False)
+        blocks = {int(h): sorted(set(rng.choice(nb, size=min(sample[1], nb), replace=False).tolist())
+                                 | {nb - 1}) for h in hs}
+    ref = oracle_outputs(w, g, osel, blocks)
+
+    # (1) the CUDA attention on the oracle's index set
+    rp, col = csr_from_masks([osel[h]["mask"] for h in range(w.hq)], nb)
+    ctx.selection_set(dims, rp, col)
+    o2 = torch.empty_like(q)
+    ctx.attend(dims, q, k, v, o2)
+    assert ctx.sync_status() == 0
+    got = o2.float().cpu().numpy()
+    worst = [0.0, 0.0, 0.0]
+    for h, bl in blocks.items():
+        r = compare_outputs(got[h][_rows(bl)], ref[h], f"attend on oracle S, head {h}")
+        worst = [max(a, b) for a, b in zip(worst, r)]
+    rep["attend_max_abs"], rep["attend_mean_abs"], rep["attend_rel_rms"] = worst
+
+    # (2) crisp_prefill's own output, for heads whose selection matched exactly
+    got_p = o.float().cpu().numpy()
+    exact = 0
+    for h, bl in blocks.items():
+        gm = np.zeros((nb, nb), bool)
+        rpg, cg = sel["row_ptr"], sel["col"]
+        for I in range(nb):
+            gm[I, cg[rpg[h * nb + I]:rpg[h * nb + I + 1]]] = True
+        if np.array_equal(gm, np.tril(osel[h]["mask"])):
+            compare_outputs(got_p[h][_rows(bl)], ref[h], f"prefill, head {h}")
+            exact += 1
+    rep["prefill_heads_compared"] = exact
+    ctx.close()
+    if report is not None:
+        report.update(rep)
+    return rep, sel, osel
+
+
+def _oracle_forced(w, g, force):
+    from oracle import crisp_oracle as O
+    params = O.workload_params(w)
+    out = {}
+    for h in range(w.hq):
+        qh = O.bf16_bits_to_f64(g["q"][h])
+        kh = O.bf16_bits_to_f64(g["k"][h // w.group])
+        out[h] = O.crisp_select_head(qh, kh, force=force, **params)
+    return out
+
+
+def test_tiny_full(dsp):
+    w = get("tiny_n4k")
+    rep, sel, osel = run_parity(dsp, w, generate(w))
+    assert sel["route_vs"].tolist() == [1, 0]
+    print("tiny_n4k", rep)
+
+
+@pytest.mark.parametrize("n,hq,hkv,seed", [(128, 2, 1, 1), (256, 2, 2, 2), (384, 4, 2, 3),
+                                          (1152, 3, 1, 4), (2176, 2, 1, 5)])
+def test_edge_shapes_random(dsp, n, hq, hkv, seed):
+    """Ragged small shapes (N_b = 1, 2, 3, 9, 17) on unplanted inputs, both routes forced."""
+    g = random_qkv(n, hq, hkv, 128, seed, scale=3.0)
+    w = Workload("edge", n=n, hq=hq, hkv=hkv, seed=seed)
+    for flags in (dsp.FLAG_FORCE_VS, dsp.FLAG_FORCE_PE, 0):
+        run_parity(dsp, w, g, flags=flags)
+
+
+@pytest.mark.parametrize("alpha,kmin,gamma", [(0.0, 0, 0.5), (1.25, 0, 0.95), (1.0, 4096, 1.0),
+                                              (3.0, 256, 0.99)])
+def test_parameter_edges(dsp, alpha, kmin, gamma):
+    w = get("tiny_n4k").with_params(alpha=alpha, k_min_tokens=kmin, gamma=gamma)
+    run_parity(dsp, w, generate(w))
+
+
+def test_llama_n32k_full(dsp):
+    w = get("llama8b_n32k")
+    rep, sel, osel = run_parity(dsp, w, generate(w))
+    assert rep["vs_heads"] + rep["pe_heads"] + rep["route_mismatch_exempt"] == w.hq
+    print("llama8b_n32k", rep)
+
+
+def test_dense_matches_oracle_and_sdpa(dsp):
+    """crisp_dense vs the oracle's dense causal attention (all blocks) on sampled rows, and
+    against torch's SDPA (a library cross-check) on every row."""
+    w = get("llama8b_n32k")
+    g = generate(w, q_heads=range(8), kv_heads=range(2))
+    w = w.with_params(hq=8, hkv=2, pe_heads=())
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    o = torch.empty_like(q)
+    ctx.dense(dims, q, k, v, o)
+    assert ctx.sync_status() == 0
+    from oracle import crisp_oracle as O
+    nb = w.n_blocks
+    full = np.tril(np.ones((nb, nb), bool))
+    got = o.float().cpu().numpy()
+    for h in (0, 5):
+        qh = O.bf16_bits_to_f64(g["q"][h])
+        kh = O.bf16_bits_to_f64(g["k"][h // 4])
+        vh = O.bf16_bits_to_f64(g["v"][h // 4])
+        bl = [0, 1, 77, nb - 1]
+        ref = O.block_sparse_attention(qh, kh, vh, full, 128, bl)
+        compare_outputs(got[h][_rows(bl)], ref, f"dense head {h}")
+    kk = k.repeat_interleave(4, dim=0)[None]
+    vv = v.repeat_interleave(4, dim=0)[None]
+    sd = torch.nn.functional.scaled_dot_product_attention(q[None], kk, vv, is_causal=True)[0]
+    d = (sd.float() - o.float()).abs()
+    assert float(d.max()) < 2e-2 and float(d.mean()) < 2e-3
+    ctx.close()
+
+
+def test_timeout_is_reported_and_context_recovers(dsp):
+    """A dropped barrier arrive makes a bounded wait run out: the kernel exits, the host
+    reads CRISP_ERR_TIMEOUT, and the next call on the same context succeeds."""
+    w = get("tiny_n4k")
+    g = generate(w)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    o = torch.empty_like(q)
+    ctx.set_debug(dsp.DEBUG_DROP_ARRIVE)
+    ctx.dense(dims, q, k, v, o)
+    assert ctx.sync_status() == 5  # CRISP_ERR_TIMEOUT
+    ctx.set_debug(0)
+    ctx.dense(dims, q, k, v, o)
+    assert ctx.sync_status() == 0
+    ref = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True)[0]
+    assert float((ref.float() - o.float()).abs().max()) < 2e-2
+    ctx.close()
+
+
+def test_api_errors(dsp):
+    w = get("tiny_n4k")
+    g = generate(w)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    o = torch.empty_like(q)
+    with pytest.raises(dsp.CrispError) as e:
+        ctx.attend(dims, q, k, v, o)
+    assert e.value.status == 7
+    big = dsp.make_dims(1, 2 * w.n, w.hq, w.hkv)
+    with pytest.raises(dsp.CrispError) as e:
+        ctx.dense(big, q, k, v, o)
+    assert e.value.status == 1
+    nb = w.n_blocks
+    rp = np.arange(w.hq * nb + 1, dtype=np.int64)
+    bad = np.tile(np.arange(nb, dtype=np.int32) + 1, w.hq)  # key block I+1 > I
+    with pytest.raises(dsp.CrispError) as e:
+        ctx.selection_set(dims, rp, bad)
+    assert e.value.status == 1
+    cfg = dsp.default_cfg(gamma=0.0)
+    with pytest.raises(dsp.CrispError) as e:
+        ctx.select(dims, q, k, cfg)
+    assert e.value.status == 1
+    ctx.close()
+
+
+@pytest.mark.parametrize("name", ["llama8b_n128k_a1", "llama8b_n128k_a125", "qwen7b_n128k"])
+def test_n128k_sampled(dsp, name):
+    w = get(name)
+    rep, _, _ = run_parity(dsp, w, generate(w), sample=(8, 16), seed=7)
+    print(name, rep)
+
+
+def test_llama_n512k_sampled_and_dense(dsp):
+    w = get("llama8b_n512k")
+    g = generate(w)
+    rep, _, osel = run_parity(dsp, w, g, sample=(8, 16), seed=11)
+    print("llama8b_n512k", rep)
+    # dense on the same inputs, sampled rows against the oracle
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    o = torch.empty_like(q)
+    ctx.dense(dims, q, k, v, o)
+    assert ctx.sync_status() == 0
+    from oracle import crisp_oracle as O
+    nb = w.n_blocks
+    full = np.tril(np.ones((nb, nb), bool))
+    got = o[[0, 31]].float().cpu().numpy()
+    for i, h in enumerate((0, 31)):
+        qh = O.bf16_bits_to_f64(g["q"][h])
+        kh = O.bf16_bits_to_f64(g["k"][h // w.group])
+        vh = O.bf16_bits_to_f64(g["v"][h // w.group])
+        bl = [3, nb // 2, nb - 1]
+        ref = O.block_sparse_attention(qh, kh, vh, full, 128, bl)
+        compare_outputs(got[i][_rows(bl)], ref, f"dense 512k head {h}")
+    ctx.close()
