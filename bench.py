@@ -345,7 +345,7 @@ def main():
     ap.add_argument("--dense-steps", type=int, default=2)
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--ref-budget", type=float, default=12.0)
     args = ap.parse_args()
     from workloads import get
     w = get(args.workload)
