@@ -24,7 +24,7 @@ DEBUG_DROP_ARRIVE = 0x1
 EXPORTED = ["crisp_cfg_default", "crisp_create", "crisp_destroy", "crisp_select", "crisp_attend",
             "crisp_prefill", "crisp_dense", "crisp_selection_get", "crisp_selection_set",
             "crisp_selection_stats", "crisp_sync_status", "crisp_set_debug",
-            "crisp_status_string", "crisp_last_error"]
+            "crisp_status_string", "crisp_last_error", "crisp_route_static"]
 
 
 class Dims(ctypes.Structure):
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "crisp_set_debug": (ctypes.c_int, [P, ctypes.c_uint32, ctypes.c_uint64]),
         "crisp_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "crisp_last_error": (ctypes.c_char_p, [P]),
+        "crisp_route_static": (ctypes.c_int, [DP, P, P, CP, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

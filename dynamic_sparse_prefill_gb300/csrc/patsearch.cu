@@ -536,3 +536,173 @@ cudaError_t init_patsearch_attributes() {
 }
 
 }  // namespace crisp
+
+// ---------------------------------------------------------------------------------------
+// crisp_route_static: the routing step with no device allocation.
+//
+// Some callers cannot call cudaMalloc: a plug-in running inside a host engine that owns
+// every byte of device memory through its own pool, or a latency-critical loop where the
+// implicit device synchronisation of an allocation is not acceptable.  This entry point
+// runs the same PatSearch kernels as crisp_select, but its scratch is the fixed array
+// below, which lives in every GPU's memory from the time the library is loaded until
+// the process exits.  It holds at most kStaticMaxHeads query heads and
+// kStaticMaxTiles (query head, key tile) pairs, i.e. batch*hq*(n/128) <= 8192: for
+// example 32 heads at 32k tokens or 8 heads at 128k tokens.  About 13 MB.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace crisp {
+namespace {
+
+constexpr int64_t kStaticMaxTiles = 8192;
+constexpr int64_t kStaticMaxHeads = 128;
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+constexpr size_t kOffStM = 0;
+constexpr size_t kOffStU = kOffStM + align256(sizeof(float) * kStaticMaxTiles * kBlk);
+constexpr size_t kOffStW = kOffStU + align256(sizeof(float) * kStaticMaxTiles * kBlk);
+constexpr size_t kOffAnc = kOffStW + align256(sizeof(float) * kStaticMaxTiles * kBlk);
+constexpr size_t kOffRowM = kOffAnc + align256(sizeof(float) * kStaticMaxHeads * 2 * kBlk);
+constexpr size_t kOffRowZ = kOffRowM + align256(sizeof(float) * kStaticMaxHeads * kBlk);
+constexpr size_t kOffPv = kOffRowZ + align256(sizeof(float) * kStaticMaxHeads * kBlk);
+constexpr size_t kOffPshi = kOffPv + align256(sizeof(float) * kStaticMaxTiles);
+constexpr size_t kOffPslo = kOffPshi + align256(sizeof(float) * kStaticMaxTiles);
+constexpr size_t kOffPs = kOffPslo + align256(sizeof(float) * kStaticMaxTiles);
+constexpr size_t kOffMu = kOffPs + align256(sizeof(float) * kStaticMaxTiles);
+constexpr size_t kOffCounts = kOffMu + align256(sizeof(float) * kStaticMaxHeads * 2);
+constexpr size_t kOffSelv = kOffCounts + align256(sizeof(int32_t) * kStaticMaxHeads * 4);
+constexpr size_t kOffSels = kOffSelv + align256(kStaticMaxTiles);
+constexpr size_t kOffErr = kOffSels + align256(kStaticMaxTiles);
+constexpr size_t kStaticBytes = kOffErr + 256;
+
+// The scratch of crisp_route_static.  In host code this name is only a stand-in: the
+// device address comes from cudaGetSymbolAddress (below) and is what the kernels get.
+static __device__ __align__(256) unsigned char g_route_scratch[kStaticBytes];
+
+struct StaticSetup {
+  bool done = false;
+  crisp_status status = CRISP_OK;
+  unsigned char* scratch = nullptr;  // device address of g_route_scratch on this device
+  EncodeTiledFn encode = nullptr;
+  int num_sms = 0;
+};
+constexpr int kMaxDevices = 64;
+StaticSetup g_static_setup[kMaxDevices];
+std::mutex g_static_mu;
+
+// Once per device, with that device current: resolve the scratch address and the other
+// per-device state.  Allocates nothing.
+crisp_status static_setup(int dev, StaticSetup** out) {
+  if (dev < 0 || dev >= kMaxDevices) return CRISP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticSetup& s = g_static_setup[dev];
+  if (!s.done) {
+    s.done = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (major != 10 || minor != 3) {
+      s.status = CRISP_ERR_UNSUPPORTED;
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.scratch), g_route_scratch) !=
+                   cudaSuccess ||
+               !s.scratch) {
+      s.status = CRISP_ERR_CUDA;
+    } else if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                cudaEnableDefault, &q) != cudaSuccess ||
+               q != cudaDriverEntryPointSuccess || !fn) {
+      s.status = CRISP_ERR_CUDA;
+    } else if (init_patsearch_attributes() != cudaSuccess) {
+      s.status = CRISP_ERR_CUDA;
+    } else {
+      s.encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (s.status != CRISP_OK) cudaGetLastError();
+  }
+  *out = &s;
+  return s.status;
+}
+
+bool static_map(EncodeTiledFn encode, CUtensorMap* map, const void* base, int64_t rows) {
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kD) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace crisp
+
+extern "C" crisp_status crisp_route_static(const crisp_dims* dims, const void* Q, const void* K,
+                                           const crisp_cfg* cfg, uint8_t* route_vs,
+                                           float* c_struct, uint32_t* status, void* stream) {
+  using namespace crisp;
+  if (!dims || !cfg || !Q || !K || !route_vs || !c_struct || !status)
+    return CRISP_ERR_INVALID_ARG;
+  if (dims->batch < 1 || dims->n < 1 || dims->hq < 1 || dims->hkv < 1 || dims->hq % dims->hkv)
+    return CRISP_ERR_INVALID_ARG;
+  if (dims->d != kD || dims->n % kBlk != 0) return CRISP_ERR_UNSUPPORTED;
+  if (cfg->B != kBlk || cfg->b != kBlk || cfg->w_sink < 1 || cfg->w_sink > kBlk ||
+      cfg->w_local < 1 || cfg->w_local > kBlk)
+    return CRISP_ERR_UNSUPPORTED;
+  if (!(cfg->alpha >= 0.f) || cfg->k_min_tokens < 0 || !(cfg->tau_proxy == cfg->tau_proxy) ||
+      ((cfg->flags & CRISP_FLAG_FORCE_VS) && (cfg->flags & CRISP_FLAG_FORCE_PE)))
+    return CRISP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K)) & 15u)
+    return CRISP_ERR_INVALID_ARG;
+  const Shape s = make_shape(*dims);
+  // Sizes beyond the static scratch are rejected before any work is queued.
+  if (s.H > kStaticMaxHeads || static_cast<int64_t>(s.H) * s.nb > kStaticMaxTiles)
+    return CRISP_ERR_UNSUPPORTED;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CRISP_ERR_CUDA;
+  StaticSetup* su = nullptr;
+  crisp_status st = static_setup(dev, &su);
+  if (st != CRISP_OK) return st;
+
+  // A context on the stack whose workspace points into the static scratch, except the
+  // two outputs, which are the caller's.
+  crisp_ctx_s c;
+  c.device = dev;
+  c.num_sms = su->num_sms;
+  c.encode = su->encode;
+  Workspace& w = c.ws;
+  unsigned char* b = su->scratch;
+  w.st_m = reinterpret_cast<float*>(b + kOffStM);
+  w.st_u = reinterpret_cast<float*>(b + kOffStU);
+  w.st_w = reinterpret_cast<float*>(b + kOffStW);
+  w.anc = reinterpret_cast<float*>(b + kOffAnc);
+  w.rowM = reinterpret_cast<float*>(b + kOffRowM);
+  w.rowZ = reinterpret_cast<float*>(b + kOffRowZ);
+  w.pv = reinterpret_cast<float*>(b + kOffPv);
+  w.pshi = reinterpret_cast<float*>(b + kOffPshi);
+  w.pslo = reinterpret_cast<float*>(b + kOffPslo);
+  w.ps = reinterpret_cast<float*>(b + kOffPs);
+  w.mu = reinterpret_cast<float*>(b + kOffMu);
+  w.counts = reinterpret_cast<int32_t*>(b + kOffCounts);
+  w.selv = b + kOffSelv;
+  w.sels = b + kOffSels;
+  w.err = reinterpret_cast<uint32_t*>(b + kOffErr);
+  w.cstruct = c_struct;
+  w.route = route_vs;
+
+  CUtensorMap tmQ, tmK;
+  if (!static_map(su->encode, &tmQ, Q, static_cast<int64_t>(s.H) * s.n) ||
+      !static_map(su->encode, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n))
+    return CRISP_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // The error word is the only scratch that must start at zero; every other scratch
+  // value is written before it is read.
+  if (cudaMemsetAsync(w.err, 0, sizeof(uint32_t), cs) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (launch_patsearch(&c, s, *cfg, tmQ, tmK, cs) != cudaSuccess) return CRISP_ERR_CUDA;
+  if (cudaMemcpyAsync(status, w.err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, cs) !=
+      cudaSuccess)
+    return CRISP_ERR_CUDA;
+  return CRISP_OK;
+}

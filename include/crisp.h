@@ -169,6 +169,30 @@ crisp_status crisp_set_debug(crisp_ctx ctx, uint32_t flags, uint64_t timeout_ns)
 
 const char* crisp_status_string(crisp_status s);
 
+/* Routing with no device allocation.  The CRISP paper has no counterpart to this call:
+ * it exists for callers that cannot call cudaMalloc -- for example a plug-in inside an
+ * engine that owns all device memory through its own pool, or a latency-critical loop
+ * that cannot afford the device synchronisation an allocation implies.
+ *
+ * Computes what the routing part of crisp_select computes (the proxy attention of the
+ * last 128 queries, C_struct and the VS/PE decision) and writes, in caller-owned device
+ * memory: route_vs[H] (1 = VS, 0 = PE), c_struct[H] (float) and status[0] (a uint32
+ * word: 0 on success, nonzero when a bounded wait ran out or a range check failed),
+ * with H = batch*hq.  Only enqueues work on `stream`; read the outputs after
+ * synchronising it.
+ *
+ * Scratch is a fixed array in the library's device memory (about 13 MB on every GPU
+ * that loads the library, held until the process exits).  Limits: batch*hq <= 128 and
+ * batch*hq*(n/128) <= 8192; larger problems return CRISP_ERR_UNSUPPORTED before any work
+ * is queued.  Other shape and parameter rules are those of crisp_select.  The first call
+ * on a device resolves the array's device address and sets kernel attributes; make
+ * that first call before any stream capture.  Every call shares the one array, so calls
+ * whose work overlaps on the GPU (two streams, or two host threads) race and give
+ * undefined results: serialise them. */
+crisp_status crisp_route_static(const crisp_dims* dims, const void* Q, const void* K,
+                                const crisp_cfg* cfg, uint8_t* route_vs, float* c_struct,
+                                uint32_t* status, void* stream);
+
 /* Text of the last CUDA error seen by this context ("" if none). */
 const char* crisp_last_error(crisp_ctx ctx);
 
