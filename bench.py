@@ -34,8 +34,9 @@ METRIC = ("sparse prefill attn ms/layer and TFLOP/s at 128k/512k; speedup vs in-
 UNIT = "ms/layer"
 B = 128
 D = 128
-# Kernel launches of one crisp_prefill: PatSearch 4, PEIndex 16, CSR 4, attention 1.
-LAUNCHES_PER_PREFILL = 25
+# Kernel launches of one crisp_prefill: PatSearch 4, PEIndex 16, CSR 4, work order 3,
+# attention 1.
+LAUNCHES_PER_PREFILL = 28
 
 
 def algorithmic_flops(nnz: int, rows: int) -> float:

@@ -7,16 +7,22 @@
 // "Method step details" step 4 applies it to the selected index set.  With every key
 // block K <= I selected this is dense causal attention, the speedup denominator.
 //
-// One CTA per (query head, query block I) work item, 6 warps:
-//   warp 0  TMA producer: Q tile once, then K_j and V_j of each selected key block into a
-//           two-stage ring;
-//   warp 1  MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers, and
-//           O += P_j V_j into the TMEM O accumulator (tcgen05, bf16 in, fp32 accumulate);
-//   warps 2-5  softmax: thread <-> query row (TMEM lane).  Online softmax in the exp2
-//           domain; the running max is only raised when a block exceeds it by more than
-//           2^8, so O is rescaled (TMEM load, scale, store) rarely; P_j is written to
-//           shared memory as bf16 in the swizzled K-major layout the MMA reads.
-// S_{j+1} is computed while the softmax works on S_j.  All waits are bounded.
+// Persistent kernel: one CTA per SM walks work items (query head h, query block I) in
+// a static round-robin over an order with the longest rows first and the heads of a
+// GQA group adjacent.  Ten warps:
+//   warps 0-3  softmax of "tile 0": the even-numbered key blocks of the item's list;
+//   warps 4-7  softmax of "tile 1": the odd-numbered key blocks;
+//   warp 8     TMA producer: the item's Q tile, then K_j into a 3-slot ring and V_j into
+//              a 2-slot ring (V one block behind K);
+//   warp 9     MMA issuer (one thread, tcgen05): S = Q K_j^T into TMEM, then
+//              O_t += P V_j with P read from TMEM.
+// The softmax warpgroups take registers from the loader warpgroup (setmaxnreg).
+// The two tiles share the item's Q tile but keep their own S buffer, running max/sum
+// and O accumulator in TMEM, so the tensor core works on one tile while the other's
+// softmax runs; the epilogue merges the two partial softmaxes exactly.  P overwrites
+// its S buffer as packed bf16.  The running max is only raised when a block exceeds it
+// by more than 2^8, so the O rescale (TMEM load, scale, store) is rare.
+// All waits are bounded (see ptx.cuh); nothing traps.
 #include <cuda_bf16.h>
 
 #include <cfloat>
@@ -27,13 +33,25 @@
 namespace crisp {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+// Warpgroups: WG0 (warps 0-3) softmax of tile 0, WG1 (warps 4-7) softmax of tile 1,
+// WG2 (warps 8-11): warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle.
+constexpr int kThreads = 384;
+// Register split: launched at kLaunchRegs per thread (the host checks the compiled
+// count), the softmax warpgroups grow to kSoftmaxRegs and WG2 shrinks to kLoaderRegs:
+// 128 * (2 * 232 + 40) = 64512 = 384 * 168.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 232;
+constexpr uint32_t kLoaderRegs = 40;
+static_assert(128 * (2 * kSoftmaxRegs + kLoaderRegs) <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);   // Q K^T
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // P V (V is MN-major)
-constexpr size_t kSmem = 1024 + kTileBytes * 2 + kStages * 2 * kTileBytes + 256;
-constexpr float kRescaleLog2 = 8.0f;  // raise the running max only past a factor 2^8
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // P V (V MN-major)
+constexpr size_t kMLBytes = 2 * 2 * kBlk * 2 * sizeof(float);         // [parity][tile][row][m,l]
+constexpr size_t kSmem = 1024 + kTileBytes * (1 + kKStages + kVStages) + kMLBytes + 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -61,15 +79,48 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 struct AttnArgs {
   int n, nb, H, hq, hkv, group;
+  int num_items;
   float scale_log2;
   const int64_t* row_ptr;  // CSR of the selection (sparse mode)
   const int32_t* col;
+  const int32_t* order;    // sparse mode: rows by descending length
   int dense;
   uint16_t* O;
   uint32_t* err;
   uint64_t timeout_ns;
   uint32_t debug;
 };
+
+struct Item {
+  int h, I, hk, L;
+  int64_t beg;
+};
+
+__device__ __forceinline__ Item get_item(const AttnArgs& a, int k) {
+  Item it;
+  if (a.dense) {
+    it.h = k % a.H;
+    it.I = a.nb - 1 - k / a.H;
+  } else {
+    const int row = a.order[k];
+    it.h = row / a.nb;
+    it.I = row % a.nb;
+  }
+  it.hk = (it.h / a.hq) * a.hkv + (it.h % a.hq) / a.group;
+  if (a.dense) {
+    it.beg = 0;
+    it.L = it.I + 1;
+  } else {
+    const int64_t row = static_cast<int64_t>(it.h) * a.nb + it.I;
+    it.beg = a.row_ptr[row];
+    it.L = static_cast<int>(a.row_ptr[row + 1] - it.beg);
+  }
+  return it;
+}
+
+__device__ __forceinline__ int block_of(const AttnArgs& a, const Item& it, int j) {
+  return a.dense ? j : a.col[it.beg + j];
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -79,50 +130,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sP = smem + kTileBytes;
-  uint8_t* sKV = smem + 2 * kTileBytes;  // stage s: K at +2s*T, V at +(2s+1)*T
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kStages * 2 * kTileBytes);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;  // [2]
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint8_t* sK = sQ + kTileBytes;
+  uint8_t* sV = sK + kKStages * kTileBytes;
+  float* sML = reinterpret_cast<float*>(sV + kVStages * kTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sML) + kMLBytes);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;    // [3]
+  uint64_t* k_empty = bars + 5;   // [3]
+  uint64_t* v_full = bars + 8;    // [2]
+  uint64_t* v_empty = bars + 10;  // [2]
+  uint64_t* s_full = bars + 12;   // [2] per tile
+  uint64_t* p_full = bars + 14;   // [2] per tile
+  uint64_t* o_done = bars + 16;
+  uint64_t* o_free = bars + 17;
+  uint64_t* ml_ready = bars + 18;
+  uint64_t* drain = bars + 19;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Work item: longest rows first (I descending), heads of a GQA group adjacent.
-  const int item = blockIdx.x;
-  const int h = item % a.H;
-  const int I = a.nb - 1 - item / a.H;
-  const int hk = (h / a.hq) * a.hkv + (h % a.hq) / a.group;
-  int64_t beg = 0;
-  int L;
-  if (a.dense) {
-    L = I + 1;
-  } else {
-    beg = a.row_ptr[static_cast<int64_t>(h) * a.nb + I];
-    L = static_cast<int>(a.row_ptr[static_cast<int64_t>(h) * a.nb + I + 1] - beg);
-  }
   const uint64_t tmo = a.timeout_ns;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 128);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+    }
     mbar_init(o_done, 1);
+    mbar_init(o_free, 256);
+    mbar_init(ml_ready, 256);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
+  if (warp == 8) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -130,198 +182,318 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_O = tmem + 256;
-
-  if (warp == 0) {
-    if (lane == 0 && L > 0) {
+  if (warp >= 8) {
+    regs_decrease<kLoaderRegs>();
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int qrow = h * a.n + I * kBlk;
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sQ, &tmQ, q_full, 0, qrow);
-      tma_load_2d(sQ + kTileBytes / 2, &tmQ, q_full, 64, qrow);
-      int issued = 0;
-      for (int j = 0; j < L; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages &&
-            !mbar_wait(&kv_empty[s], ((j / kStages) + 1) & 1, a.err, abort_flag, tmo))
-          break;
-        int kb = a.dense ? j : a.col[beg + j];
-        if (kb < 0 || kb > I) {
-          atomicOr(a.err, kErrRange);
-          kb = I;
-        }
-        const int krow = hk * a.n + kb * kBlk;
-        uint8_t* dK = sKV + (2 * s) * kTileBytes;
-        uint8_t* dV = dK + kTileBytes;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * kTileBytes);
-        tma_load_2d(dK, &tmK, &kv_full[s], 0, krow);
-        tma_load_2d(dK + kTileBytes / 2, &tmK, &kv_full[s], 64, krow);
-        tma_load_2d(dV, &tmV, &kv_full[s], 0, krow);
-        tma_load_2d(dV + kTileBytes / 2, &tmV, &kv_full[s], 64, krow);
-        ++issued;
-      }
-      drain_wait(q_full, 0, a.err, tmo);
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        drain_wait(&kv_full[j % kStages], (j / kStages) & 1, a.err, tmo);
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && L > 0) {
-      const uint32_t q_base = smem_u32(sQ);
-      const uint32_t p_base = smem_u32(sP);
-      auto issue_s = [&](int j) {
-        const int s = j % kStages;
-        const uint32_t k_base = smem_u32(sKV + (2 * s) * kTileBytes);
-        const uint32_t d = tmem + (j & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          umma_bf16(d, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
-                    kIdescS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[j & 1]);
+      int gk = 0, gv = 0, item_idx = 0, q_loads = 0;
+      bool ok = true;
+      auto load_v = [&](int hk, int kb) -> bool {
+        const int s = gv % kVStages;
+        if (gv >= kVStages &&
+            !mbar_wait(&v_empty[s], ((gv / kVStages) + 1) & 1, a.err, abort_flag, tmo))
+          return false;
+        uint8_t* dst = sV + s * kTileBytes;
+        const int row = hk * a.n + kb * kBlk;
+        mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+        tma_load_2d(dst, &tmV, &v_full[s], 0, row);
+        tma_load_2d(dst + kTileBytes / 2, &tmV, &v_full[s], 64, row);
+        ++gv;
+        return true;
       };
-      bool ok = mbar_wait(q_full, 0, a.err, abort_flag, tmo) &&
-                mbar_wait(&kv_full[0], 0, a.err, abort_flag, tmo);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        for (int j = 0; j < L; ++j) {
-          if (j + 1 < L) {
-            if (!mbar_wait(&kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, a.err,
-                           abort_flag, tmo))
-              break;
-            tc_fence_after();
-            issue_s(j + 1);
+      for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
+        const Item it = get_item(a, k);
+        if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        const int qrow = it.h * a.n + it.I * kBlk;
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        tma_load_2d(sQ, &tmQ, q_full, 0, qrow);
+        tma_load_2d(sQ + kTileBytes / 2, &tmQ, q_full, 64, qrow);
+        ++q_loads;
+        int kb_prev = 0;
+        for (int j = 0; j < it.L; ++j) {
+          int kb = block_of(a, it, j);
+          if (kb < 0 || kb > it.I) {
+            atomicOr(a.err, kErrRange);
+            kb = it.I;
           }
-          if (!mbar_wait(p_full, j & 1, a.err, abort_flag, tmo)) break;
+          const int s = gk % kKStages;
+          if (gk >= kKStages &&
+              !mbar_wait(&k_empty[s], ((gk / kKStages) + 1) & 1, a.err, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = sK + s * kTileBytes;
+          const int row = it.hk * a.n + kb * kBlk;
+          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+          tma_load_2d(dst, &tmK, &k_full[s], 0, row);
+          tma_load_2d(dst + kTileBytes / 2, &tmK, &k_full[s], 64, row);
+          ++gk;
+          if (j >= 1 && !load_v(it.hk, kb_prev)) {
+            ok = false;
+            break;
+          }
+          kb_prev = kb;
+        }
+        if (ok && it.L > 0 && !load_v(it.hk, kb_prev)) ok = false;
+      }
+      // Let every copy still in flight land before the CTA can exit.
+      if (q_loads > 0) drain_wait(q_full, (q_loads - 1) & 1, a.err, tmo);
+      for (int g = max(0, gk - kKStages); g < gk; ++g)
+        drain_wait(&k_full[g % kKStages], (g / kKStages) & 1, a.err, tmo);
+      for (int g = max(0, gv - kVStages); g < gv; ++g)
+        drain_wait(&v_full[g % kVStages], (g / kVStages) & 1, a.err, tmo);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_base = smem_u32(sQ);
+      int gk = 0, gv = 0, item_idx = 0;
+      int cnt[2] = {0, 0};
+      bool ok = true;
+      for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
+        const Item it = get_item(a, k);
+        if (!mbar_wait(q_full, item_idx & 1, a.err, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        bool first_pv = true;
+        auto do_pv = [&](int jj) -> bool {
+          const int tt = jj & 1;
+          if (!mbar_wait(&p_full[tt], cnt[tt] & 1, a.err, abort_flag, tmo)) return false;
+          ++cnt[tt];
+          if (first_pv) {
+            if (item_idx > 0 &&
+                !mbar_wait(o_free, (item_idx - 1) & 1, a.err, abort_flag, tmo))
+              return false;
+            first_pv = false;
+          }
+          const int s = gv % kVStages;
+          if (!mbar_wait(&v_full[s], (gv / kVStages) & 1, a.err, abort_flag, tmo)) return false;
           tc_fence_after();
-          const int s = j % kStages;
-          const uint32_t v_base = smem_u32(sKV + (2 * s + 1) * kTileBytes);
+          const uint32_t v_base = smem_u32(sV + s * kTileBytes);
+          const uint32_t d = tmem + 256 + tt * 128;
+          const uint32_t p = tmem + tt * 128;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-            // B = V_j rows kk*16.. (keys), MN-major: 64-column regions 16 KB apart (LBO),
-            // 8-row groups 1024 B apart (SBO).
-            umma_bf16(tmem_O, sdesc_sw128(p_base + aoff, 16, 1024),
-                      sdesc_sw128(v_base + kk * 2048, kTileBytes / 2, 1024), kIdescPV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+            // B = V rows 16kk.. (keys): MN-major, 64-column regions 16 KB apart (LBO),
+            // 8-row groups 1024 B apart (SBO).  A = P from TMEM, 8 columns per K step.
+            umma_bf16_tmem_a(d, p + kk * 8, sdesc_sw128(v_base + kk * 2048, kTileBytes / 2, 1024),
+                             kIdescPV, (jj >= 2 || kk > 0) ? 1u : 0u);
           }
+          umma_commit(&v_empty[s]);
+          ++gv;
+          return true;
+        };
+        for (int j = 0; j < it.L && ok; ++j) {
+          const int t = j & 1;
+          const int s = gk % kKStages;
+          if (!mbar_wait(&k_full[s], (gk / kKStages) & 1, a.err, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(sK + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+            umma_bf16(tmem + t * 128, sdesc_sw128(q_base + off, 16, 1024),
+                      sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[t]);
+          umma_commit(&k_empty[s]);
+          ++gk;
+          if (j == it.L - 1) umma_commit(q_empty);
+          if (j >= 1 && !do_pv(j - 1)) ok = false;
+        }
+        if (ok && it.L > 0) {
+          if (!do_pv(it.L - 1)) ok = false;
           umma_commit(o_done);
-          umma_commit(&kv_empty[s]);
         }
       }
       umma_commit(drain);
       drain_wait(drain, 0, a.err, tmo);
     }
+  }
   } else {
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
+    regs_increase<kSoftmaxRegs>();
+    // ------------------------------------------------------------------ softmax / epilogue
+    const int t = warp >> 2;         // tile: 0 for warps 0-3, 1 for warps 4-7
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;     // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    uint16_t* orow = a.O + (static_cast<size_t>(h) * a.n + static_cast<size_t>(I) * kBlk + r) * kD;
-    float m_run = -FLT_MAX, l_run = 0.f;
-    bool ok = L > 0;
-    for (int j = 0; j < L && ok; ++j) {
-      if (!warp_wait(&s_full[j & 1], (j >> 1) & 1, a.err, abort_flag, tmo)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t v[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + (j & 1) * 128 + c * 32, v[c]);
-      const int kb = a.dense ? j : a.col[beg + j];
-      const bool diag = (kb == I);
-      float mloc = -FLT_MAX;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float s2 = __uint_as_float(v[c4][c]) * a.scale_log2;
-          if (diag && (c4 * 32 + c) > r) s2 = -FLT_MAX;
-          v[c4][c] = __float_as_uint(s2);
-          mloc = fmaxf(mloc, s2);
+    const uint32_t s_addr = tmem + lane_off + t * 128;
+    const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
+    int ns = 0, item_idx = 0;
+    bool ok = true;
+    for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
+      const Item it = get_item(a, k);
+      float m_run = -FLT_MAX, l_run = 0.f;
+      for (int jj = t; jj < it.L; jj += 2) {
+        if (!warp_wait(&s_full[t], ns & 1, a.err, abort_flag, tmo)) {
+          ok = false;
+          break;
         }
-      float alpha = 1.f;
-      if (mloc > m_run + kRescaleLog2 || j == 0) {
-        const float m_new = fmaxf(m_run, mloc);
-        alpha = (j == 0) ? 0.f : fast_exp2(m_run - m_new);
-        m_run = m_new;
-      }
-      float rs = 0.f;
-      uint32_t pk[4][16];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float s0 = __uint_as_float(v[c4][2 * c]);
-          const float s1 = __uint_as_float(v[c4][2 * c + 1]);
-          const float p0 = s0 == -FLT_MAX ? 0.f : fast_exp2(s0 - m_run);
-          const float p1 = s1 == -FLT_MAX ? 0.f : fast_exp2(s1 - m_run);
-          rs += p0 + p1;
-          pk[c4][c] = pack_bf16(p0, p1);
-        }
-      l_run = l_run * alpha + rs;
-      if (j > 0 && !warp_wait(o_done, (j - 1) & 1, a.err, abort_flag, tmo)) {
-        ok = false;
-        break;
-      }
-      // P_j -> shared memory, 128-byte swizzled K-major (keys are the K dimension).
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        const uint32_t off = (c16 >> 3) * (kTileBytes / 2) + r * 128 +
-                             ((static_cast<uint32_t>(c16 & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sP + off) =
-            make_uint4(pk[c16 >> 2][(c16 & 3) * 4 + 0], pk[c16 >> 2][(c16 & 3) * 4 + 1],
-                       pk[c16 >> 2][(c16 & 3) * 4 + 2], pk[c16 >> 2][(c16 & 3) * 4 + 3]);
-      }
-      fence_proxy_async_smem();
-      if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
+        ++ns;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem_O + lane_off + c * 32, o);
+        const bool diag = block_of(a, it, jj) == it.I;
+        // The whole S row in one TMEM round trip; P is packed in place (pair c from
+        // elements 2c, 2c+1, which are read before index c is overwritten).
+        uint32_t v[128];
+        tmem_ld128(s_addr, v);
+        float mloc = -FLT_MAX;
+        if (diag) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          tmem_st32(tmem_O + lane_off + c * 32, o);
+          for (int c = 0; c < 128; ++c)
+            if (c <= r) mloc = fmaxf(mloc, __uint_as_float(v[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) mloc = fmaxf(mloc, __uint_as_float(v[c]));
+        }
+        const float ms = mloc * a.scale_log2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (jj == t) {
+          m_run = ms;
+        } else if (ms > m_run + kRescaleLog2) {
+          alpha = fast_exp2(m_run - ms);
+          m_run = ms;
+          rescale = true;
+        }
+        const float neg = -m_run;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * c]), a.scale_log2, neg));
+          float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * c + 1]), a.scale_log2, neg));
+          if (diag) {
+            p0 = 2 * c <= r ? p0 : 0.f;
+            p1 = 2 * c + 1 <= r ? p1 : 0.f;
+          }
+          rs += p0 + p1;
+          v[c] = pack_bf16(p0, p1);
+        }
+        tmem_st64p(s_addr, v);
+        l_run = l_run * alpha + rs;
+        // s_full of this block implies the tile's previous P.V has completed, so O may
+        // be rescaled here without another wait.
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c * 32, o);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+            tmem_st32(o_addr + c * 32, o);
+          }
         }
         tmem_st_wait();
+        tc_fence_before();
+        const bool drop = (a.debug & CRISP_DEBUG_DROP_ARRIVE) && blockIdx.x == 0 &&
+                          item_idx == 0 && jj + 2 >= it.L;
+        if (!drop) mbar_arrive(&p_full[t]);
       }
-      tc_fence_before();
-      const bool drop = (a.debug & CRISP_DEBUG_DROP_ARRIVE) && blockIdx.x == 0 && j == L - 1;
-      if (!drop) mbar_arrive(p_full);
-    }
-    if (ok && warp_wait(o_done, (L - 1) & 1, a.err, abort_flag, tmo)) {
+      if (!ok) break;
+      // ---- epilogue: merge the two tiles' partial softmaxes, write this tile's half
+      const int par = item_idx & 1;
+      float* my = sML + ((par * 2 + t) * kBlk + r) * 2;
+      const float* other = sML + ((par * 2 + (t ^ 1)) * kBlk + r) * 2;
+      my[0] = m_run;
+      my[1] = l_run;
+      mbar_arrive(ml_ready);
+      if (!warp_wait(ml_ready, item_idx & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      const float m_o = other[0], l_o = other[1];
+      if (!warp_wait(o_done, item_idx & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float mA = t == 0 ? m_run : m_o, lA = t == 0 ? l_run : l_o;
+      const float mB = t == 0 ? m_o : m_run, lB = t == 0 ? l_o : l_run;
+      const bool hasB = it.L >= 2;
+      const float m = hasB ? fmaxf(mA, mB) : mA;
+      const float aA = fast_exp2(mA - m);
+      const float aB = hasB ? fast_exp2(mB - m) : 0.f;
+      const float inv = 1.f / (lA * aA + lB * aB);
+      const float wA = aA * inv, wB = aB * inv;
+      uint16_t* orow = a.O + (static_cast<size_t>(it.h) * a.n + static_cast<size_t>(it.I) * kBlk + r) * kD + t * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem_O + lane_off + c * 32, o);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t oa[32], ob[32];
+        tmem_ld32(tmem + lane_off + 256 + t * 64 + hh * 32, oa);
+        if (hasB) tmem_ld32(tmem + lane_off + 384 + t * 64 + hh * 32, ob);
 #pragma unroll
-        for (int k = 0; k < 32; k += 8) {
+        for (int c = 0; c < 32; c += 8) {
+          float f[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            f[x] = __uint_as_float(oa[c + x]) * wA + (hasB ? __uint_as_float(ob[c + x]) * wB : 0.f);
           uint4 pkt;
-          pkt.x = pack_bf16(__uint_as_float(o[k + 0]) * inv_l, __uint_as_float(o[k + 1]) * inv_l);
-          pkt.y = pack_bf16(__uint_as_float(o[k + 2]) * inv_l, __uint_as_float(o[k + 3]) * inv_l);
-          pkt.z = pack_bf16(__uint_as_float(o[k + 4]) * inv_l, __uint_as_float(o[k + 5]) * inv_l);
-          pkt.w = pack_bf16(__uint_as_float(o[k + 6]) * inv_l, __uint_as_float(o[k + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(orow + c * 32 + k) = pkt;
+          pkt.x = pack_bf16(f[0], f[1]);
+          pkt.y = pack_bf16(f[2], f[3]);
+          pkt.z = pack_bf16(f[4], f[5]);
+          pkt.w = pack_bf16(f[6], f[7]);
+          *reinterpret_cast<uint4*>(orow + hh * 32 + c) = pkt;
         }
       }
-    } else {
-      // No output could be formed (empty row or an aborted wait): write zeros.
-      for (int k = 0; k < kD; k += 8) *reinterpret_cast<uint4*>(orow + k) = make_uint4(0, 0, 0, 0);
-      if (L <= 0) atomicOr(a.err, kErrRange);
+      tc_fence_before();
+      mbar_arrive(o_free);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Counting sort of the selection's rows by descending length (longest first): the
+// attention kernel's CTAs take rows round-robin from this order, so every SM gets a
+// similar share of the work.  Rows of equal length keep no particular order.
+__global__ void order_hist_kernel(const int64_t* __restrict__ row_ptr, int rows, int* hist) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row < rows) atomicAdd(&hist[row_ptr[row + 1] - row_ptr[row]], 1);
+}
+
+__global__ void __launch_bounds__(1024) order_scan_kernel(int* hist, int nb) {
+  // cursor[len] = number of rows longer than len, for len in [0, nb]
+  __shared__ int part[1024];
+  const int nbins = nb + 1;
+  const int per = (nbins + 1023) / 1024;
+  // bins in descending length: position p holds length nb - p
+  const int p0 = threadIdx.x * per, p1 = min(nbins, p0 + per);
+  int s = 0;
+  for (int p = p0; p < p1; ++p) s += hist[nb - p];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int t = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += t;
+    __syncthreads();
+  }
+  int run = part[threadIdx.x] - s;
+  for (int p = p0; p < p1; ++p) {
+    const int c = hist[nb - p];
+    hist[nb - p] = run;
+    run += c;
+  }
+}
+
+__global__ void order_scatter_kernel(const int64_t* __restrict__ row_ptr, int rows, int* cursor,
+                                     int32_t* order) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row < rows) order[atomicAdd(&cursor[row_ptr[row + 1] - row_ptr[row]], 1)] = row;
 }
 
 }  // namespace
@@ -336,20 +508,37 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.hq = s.hq;
   a.hkv = s.hkv;
   a.group = s.group;
+  a.num_items = s.H * s.nb;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
   a.row_ptr = ctx->ws.row_ptr;
   a.col = ctx->ws.col;
+  a.order = ctx->ws.order;
   a.dense = dense ? 1 : 0;
+  if (!dense) {
+    const int rows = s.H * s.nb;
+    cudaError_t e = cudaMemsetAsync(ctx->ws.len_hist, 0, sizeof(int) * (s.nb + 2), st);
+    if (e != cudaSuccess) return e;
+    order_hist_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows, ctx->ws.len_hist);
+    order_scan_kernel<<<1, 1024, 0, st>>>(ctx->ws.len_hist, s.nb);
+    order_scatter_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows,
+                                                              ctx->ws.len_hist, ctx->ws.order);
+  }
   a.O = static_cast<uint16_t*>(O);
   a.err = ctx->ws.err;
   a.timeout_ns = (ctx->debug_flags & CRISP_DEBUG_DROP_ARRIVE) ? 50000000ull : ctx->timeout_ns;
   a.debug = ctx->debug_flags;
-  const unsigned items = static_cast<unsigned>(s.H) * static_cast<unsigned>(s.nb);
-  attention_kernel<<<items, kThreads, kSmem, st>>>(tmQ, tmK, tmV, a);
+  const int grid = a.num_items < ctx->num_sms ? a.num_items : ctx->num_sms;
+  attention_kernel<<<grid, kThreads, kSmem, st>>>(tmQ, tmK, tmV, a);
   return cudaGetLastError();
 }
 
 cudaError_t init_attention_attributes() {
+  // setmaxnreg.inc waits until the registers it asks for are free, so the split must fit
+  // in what the CTA is launched with: refuse to run a build whose count differs.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel);
+  if (e != cudaSuccess) return e;
+  if (static_cast<uint32_t>(fa.numRegs) != kLaunchRegs) return cudaErrorInvalidKernelImage;
   return cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmem));
 }

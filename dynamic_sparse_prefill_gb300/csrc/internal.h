@@ -57,6 +57,9 @@ struct Workspace {
   int64_t* row_ptr = nullptr;   // [H*nb+1]
   int32_t* col = nullptr;       // [col_cap]
   int64_t col_cap = 0;
+  // attention work order: rows sorted by descending length (counting sort)
+  int32_t* order = nullptr;     // [H*nb]
+  int32_t* len_hist = nullptr;  // [nb+2] histogram, then cursors
   uint32_t* err = nullptr;      // device error word
 };
 
