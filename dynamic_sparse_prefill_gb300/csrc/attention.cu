@@ -347,15 +347,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // elements 2c, 2c+1, which are read before index c is overwritten).
         uint32_t v[128];
         tmem_ld128(s_addr, v);
-        float mloc = -FLT_MAX;
+        // eight independent max chains instead of one serial chain of 128
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -FLT_MAX;
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c <= r) mloc = fmaxf(mloc, __uint_as_float(v[c]));
+            if (c <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
         } else {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mloc = fmaxf(mloc, __uint_as_float(v[c]));
+          for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
         }
+        const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float ms = mloc * a.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
@@ -367,7 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float neg = -m_run;
-        float rs = 0.f;
+        float sm[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sm[i] = 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * c]), a.scale_log2, neg));
@@ -376,9 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             p0 = 2 * c <= r ? p0 : 0.f;
             p1 = 2 * c + 1 <= r ? p1 : 0.f;
           }
-          rs += p0 + p1;
+          sm[c & 7] += p0 + p1;
           v[c] = pack_bf16(p0, p1);
         }
+        const float rs = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
         tmem_st64p(s_addr, v);
         l_run = l_run * alpha + rs;
         // s_full of this block implies the tile's previous P.V has completed, so O may

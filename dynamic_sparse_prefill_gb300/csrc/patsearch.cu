@@ -180,34 +180,54 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       const int t = t_begin + i;
       const bool last = (t == a.nb - 1);
       const int j0 = t * kBlk;
-      float mx = -FLT_MAX;
+      // Row maximum over the tile's visible keys (the last tile is causal: c <= r),
+      // eight independent chains.
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -FLT_MAX;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int col = c4 * 32 + c;
-          const float s2 = __uint_as_float(v[c4][c]) * a.scale_log2;
-          if (!last || col <= r) mx = fmaxf(mx, s2);
+          if (!last || col <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c4][c]));
         }
-      float u = 0.f, w = 0.f, an = 0.f;
+      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m2 = mraw * a.scale_log2;
+      const float neg = -m2;
+      // u: keys with c <= r (slash block N_b-1-t), w: keys with c > r (slash block N_b-2-t)
+      float uu[4] = {0.f, 0.f, 0.f, 0.f}, ww[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int col = c4 * 32 + c;
-          const float s2 = __uint_as_float(v[c4][c]) * a.scale_log2;
-          const bool valid = !last || col <= r;
-          const float e = valid ? fast_exp2(s2 - mx) : 0.f;
+          const float e = fast_exp2(fmaf(__uint_as_float(v[c4][c]), a.scale_log2, neg));
           if (col <= r)
-            u += e;
-          else
-            w += e;
-          const int j = j0 + col;
-          const bool anchor = (t == 0 && j < a.w_sink) || (last && j >= a.n - a.w_local);
-          if (anchor) an += e;
+            uu[c & 3] += e;
+          else if (!last)
+            ww[c & 3] += e;
         }
+      const float u = (uu[0] + uu[1]) + (uu[2] + uu[3]);
+      const float w = (ww[0] + ww[1]) + (ww[2] + ww[3]);
+      // Anchor mass: the first w_sink keys (tile 0) and the last w_local keys (last tile).
+      float an = 0.f;
+      if (t == 0 || last) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int col = c4 * 32 + c;
+            const int j = j0 + col;
+            const bool valid = !last || col <= r;
+            const bool anchor = (t == 0 && j < a.w_sink) || (last && j >= a.n - a.w_local);
+            if (valid && anchor) an += fast_exp2(fmaf(__uint_as_float(v[c4][c]), a.scale_log2, neg));
+          }
+      }
+      const float mx_out = m2;
       const size_t idx = (static_cast<size_t>(h) * a.nb + t) * kBlk + r;
-      a.st_m[idx] = mx;
+      a.st_m[idx] = mx_out;
       a.st_u[idx] = u;
       a.st_w[idx] = w;
       if (t == 0) {

@@ -195,33 +195,34 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
   scnt[threadIdx.x] = 0;
   smass[threadIdx.x] = 0.0;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
+  // Each thread keeps a run (bin, count, fp32 mass) and flushes it to the shared
+  // histogram only when the bin changes: the early passes see long runs of one bin.
+  uint32_t cur = 0xFFFFFFFFu, cnt = 0;
+  float mass = 0.f;
   const int I0 = blockIdx.x * kHistRows;
   for (int I = I0; I < min(nb, I0 + kHistRows); ++I) {
     const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
-    for (int K0 = 0; K0 <= I; K0 += 256) {
-      const int K = K0 + threadIdx.x;
-      const bool valid = K <= I;
-      const float v = valid ? row[K] : 0.f;
+    for (int K = threadIdx.x; K <= I; K += 256) {
+      const float v = row[K];
       const uint32_t bits = __float_as_uint(v);
-      const bool take = valid && ((bits & st.decided) == st.prefix);
-      const unsigned act = __ballot_sync(0xffffffffu, take);
-      if (take) {
-        const uint32_t bin = (bits >> shift) & 255u;
-        const unsigned grp = __match_any_sync(act, bin);
-        double total = 0.0;
-        unsigned mm = grp;
-        while (mm) {
-          const int src = __ffs(mm) - 1;
-          total += __shfl_sync(grp, static_cast<double>(v), src);
-          mm &= mm - 1;
+      if ((bits & st.decided) != st.prefix) continue;
+      const uint32_t bin = (bits >> shift) & 255u;
+      if (bin != cur) {
+        if (cnt) {
+          atomicAdd(&scnt[cur], cnt);
+          atomicAdd(&smass[cur], static_cast<double>(mass));
         }
-        if (lane == __ffs(grp) - 1) {
-          atomicAdd(&scnt[bin], static_cast<unsigned>(__popc(grp)));
-          atomicAdd(&smass[bin], total);
-        }
+        cur = bin;
+        cnt = 0;
+        mass = 0.f;
       }
+      ++cnt;
+      mass += v;
     }
+  }
+  if (cnt) {
+    atomicAdd(&scnt[cur], cnt);
+    atomicAdd(&smass[cur], static_cast<double>(mass));
   }
   __syncthreads();
   if (scnt[threadIdx.x]) {
