@@ -12,10 +12,10 @@
 // GQA group adjacent.  Ten warps:
 //   warps 0-3  softmax of "tile 0": the even-numbered key blocks of the item's list;
 //   warps 4-7  softmax of "tile 1": the odd-numbered key blocks;
-//   warp 8     TMA producer: the item's Q tile, then K_j into a 3-slot ring and V_j into
-//              a 2-slot ring (V one block behind K);
+//   warp 8     TMA producer of the item's Q tile and K_j (3-slot ring);
 //   warp 9     MMA issuer (one thread, tcgen05): S = Q K_j^T into TMEM, then
-//              O_t += P V_j with P read from TMEM.
+//              O_t += P V_j with P read from TMEM;
+//   warp 10    TMA producer of V_j (2-slot ring), so K prefetch never waits on a V slot.
 // The softmax warpgroups take registers from the loader warpgroup (setmaxnreg).
 // The two tiles share the item's Q tile but keep their own S buffer, running max/sum
 // and O accumulator in TMEM, so the tensor core works on one tile while the other's
@@ -34,7 +34,7 @@ namespace crisp {
 namespace {
 
 // Warpgroups: WG0 (warps 0-3) softmax of tile 0, WG1 (warps 4-7) softmax of tile 1,
-// WG2 (warps 8-11): warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle.
+// WG2 (warps 8-11): warp 8 Q/K producer, warp 9 MMA issuer, warp 10 V producer.
 constexpr int kThreads = 384;
 // Register split: launched at kLaunchRegs per thread (the host checks the compiled
 // count), the softmax warpgroups grow to kSoftmaxRegs and WG2 shrinks to kLoaderRegs:
@@ -51,6 +51,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // P V (V
 constexpr size_t kMLBytes = 2 * 2 * kBlk * 2 * sizeof(float);         // [parity][tile][row][m,l]
 constexpr size_t kSmem = 1024 + kTileBytes * (1 + kKStages + kVStages) + kMLBytes + 512;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLazySum = 32768.0f;  // 128 columns x 2^8
 constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -75,6 +76,62 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Packed two-lane fp32 arithmetic (one instruction for two values).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Row maximum of the 128 raw logits of an S row (columns c > r masked on the diagonal).
+template <bool kDiag>
+__device__ __forceinline__ float row_max(const uint32_t (&v)[128], int r) {
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = -FLT_MAX;
+#pragma unroll
+  for (int c = 0; c < 128; ++c)
+    if (!kDiag || c <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
+  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
+// P = exp2(s * scale - m) for the 128 columns of an S row, packed to bf16 pairs in place
+// (v[c] <- (p[2c], p[2c+1]); elements 2c, 2c+1 are read before index c is written).
+// Returns the row sum of P.
+template <bool kDiag>
+__device__ __forceinline__ float exp_pack(uint32_t (&v)[128], float scale, float m, int r) {
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const float neg = -m;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    float x0, x1;
+    ffma2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), scale, scale, neg, neg);
+    if (kDiag) {
+      x0 = 2 * c <= r ? x0 : -INFINITY;
+      x1 = 2 * c + 1 <= r ? x1 : -INFINITY;
+    }
+    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+    const int a = (c & 3) * 2;
+    fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
+    v[c] = pack_bf16(p0, p1);
+  }
+  fadd2(acc[0], acc[1], acc[0], acc[1], acc[2], acc[3]);
+  fadd2(acc[4], acc[5], acc[4], acc[5], acc[6], acc[7]);
+  fadd2(acc[0], acc[1], acc[0], acc[1], acc[4], acc[5]);
+  return acc[0] + acc[1];
 }
 
 struct AttnArgs {
@@ -185,26 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
     regs_decrease<kLoaderRegs>();
   if (warp == 8) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer: Q, K
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      int gk = 0, gv = 0, item_idx = 0, q_loads = 0;
+      int gk = 0, item_idx = 0, q_loads = 0;
       bool ok = true;
-      auto load_v = [&](int hk, int kb) -> bool {
-        const int s = gv % kVStages;
-        if (gv >= kVStages &&
-            !mbar_wait(&v_empty[s], ((gv / kVStages) + 1) & 1, a.err, abort_flag, tmo))
-          return false;
-        uint8_t* dst = sV + s * kTileBytes;
-        const int row = hk * a.n + kb * kBlk;
-        mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-        tma_load_2d(dst, &tmV, &v_full[s], 0, row);
-        tma_load_2d(dst + kTileBytes / 2, &tmV, &v_full[s], 64, row);
-        ++gv;
-        return true;
-      };
       for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
         const Item it = get_item(a, k);
         if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) {
@@ -216,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sQ, &tmQ, q_full, 0, qrow);
         tma_load_2d(sQ + kTileBytes / 2, &tmQ, q_full, 64, qrow);
         ++q_loads;
-        int kb_prev = 0;
         for (int j = 0; j < it.L; ++j) {
           int kb = block_of(a, it, j);
           if (kb < 0 || kb > it.I) {
@@ -235,18 +277,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(dst, &tmK, &k_full[s], 0, row);
           tma_load_2d(dst + kTileBytes / 2, &tmK, &k_full[s], 64, row);
           ++gk;
-          if (j >= 1 && !load_v(it.hk, kb_prev)) {
-            ok = false;
-            break;
-          }
-          kb_prev = kb;
         }
-        if (ok && it.L > 0 && !load_v(it.hk, kb_prev)) ok = false;
       }
       // Let every copy still in flight land before the CTA can exit.
       if (q_loads > 0) drain_wait(q_full, (q_loads - 1) & 1, a.err, tmo);
       for (int g = max(0, gk - kKStages); g < gk; ++g)
         drain_wait(&k_full[g % kKStages], (g / kKStages) & 1, a.err, tmo);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ TMA producer: V
+    if (lane == 0) {
+      tma_prefetch_desc(&tmV);
+      int gv = 0;
+      bool ok = true;
+      for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x) {
+        const Item it = get_item(a, k);
+        for (int j = 0; j < it.L; ++j) {
+          int kb = block_of(a, it, j);
+          if (kb < 0 || kb > it.I) kb = it.I;
+          const int s = gv % kVStages;
+          if (gv >= kVStages &&
+              !mbar_wait(&v_empty[s], ((gv / kVStages) + 1) & 1, a.err, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = sV + s * kTileBytes;
+          const int row = it.hk * a.n + kb * kBlk;
+          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+          tma_load_2d(dst, &tmV, &v_full[s], 0, row);
+          tma_load_2d(dst + kTileBytes / 2, &tmV, &v_full[s], 64, row);
+          ++gv;
+        }
+      }
       for (int g = max(0, gv - kVStages); g < gv; ++g)
         drain_wait(&v_full[g % kVStages], (g / kVStages) & 1, a.err, tmo);
     }
@@ -343,52 +405,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++ns;
         tc_fence_after();
         const bool diag = block_of(a, it, jj) == it.I;
-        // The whole S row in one TMEM round trip; P is packed in place (pair c from
-        // elements 2c, 2c+1, which are read before index c is overwritten).
+        const bool first = (jj == t);
+        // The whole S row in one TMEM round trip.
         uint32_t v[128];
         tmem_ld128(s_addr, v);
-        // eight independent max chains instead of one serial chain of 128
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -FLT_MAX;
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
-        }
-        const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float ms = mloc * a.scale_log2;
-        float alpha = 1.f;
+        float alpha = 1.f, rs = 0.f;
         bool rescale = false;
-        if (jj == t) {
-          m_run = ms;
-        } else if (ms > m_run + kRescaleLog2) {
-          alpha = fast_exp2(m_run - ms);
-          m_run = ms;
-          rescale = true;
+        // Fast path: exponentiate against the running max without recomputing the row
+        // maximum; accepted while every P stays below kLazySum.  Otherwise (and for the
+        // tile's first block of the item) reload S, take the exact row maximum and raise
+        // the running max when the block exceeds it by more than 2^kRescaleLog2.
+        bool slow = first;
+        if (!first) {
+          rs = diag ? exp_pack<true>(v, a.scale_log2, m_run, r)
+                    : exp_pack<false>(v, a.scale_log2, m_run, r);
+          slow = __any_sync(0xffffffffu, !(rs <= kLazySum));
+          if (slow) tmem_ld128(s_addr, v);
         }
-        const float neg = -m_run;
-        float sm[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sm[i] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * c]), a.scale_log2, neg));
-          float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * c + 1]), a.scale_log2, neg));
-          if (diag) {
-            p0 = 2 * c <= r ? p0 : 0.f;
-            p1 = 2 * c + 1 <= r ? p1 : 0.f;
+        if (slow) {
+          const float ms = (diag ? row_max<true>(v, r) : row_max<false>(v, r)) * a.scale_log2;
+          if (first) {
+            m_run = ms;
+          } else if (ms > m_run + kRescaleLog2) {
+            alpha = fast_exp2(m_run - ms);
+            m_run = ms;
+            rescale = true;
           }
-          sm[c & 7] += p0 + p1;
-          v[c] = pack_bf16(p0, p1);
+          rs = diag ? exp_pack<true>(v, a.scale_log2, m_run, r)
+                    : exp_pack<false>(v, a.scale_log2, m_run, r);
         }
-        const float rs = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-        tmem_st64p(s_addr, v);
         l_run = l_run * alpha + rs;
+        tmem_st64p(s_addr, v);
         // s_full of this block implies the tile's previous P.V has completed, so O may
         // be rescaled here without another wait.
         if (__any_sync(0xffffffffu, rescale)) {
