@@ -220,8 +220,10 @@ def run_gpu(args, w, rank, world):
     o = torch.empty_like(q)
     dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
     ctx = dsp.Context(dims)
+    flags = {"none": 0, "median": dsp.FLAG_MEDIAN_FLOOR,
+             "gamma": dsp.FLAG_VS_GAMMA_CUMSUM}[args.vs_variant]
     cfg = dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy,
-                          k_min_tokens=w.k_min_tokens)
+                          k_min_tokens=w.k_min_tokens, flags=flags)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -310,7 +312,7 @@ def run_gpu(args, w, rank, world):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (planted, seeded); no real-model activations",
-        "config": workload_config(w),
+        "config": dict(workload_config(w), vs_variant=args.vs_variant),
         "tflops_effective": flops / (ms_per_step * 1e-3) / 1e12,
         "select_ms": sel_ms, "attend_ms": att_ms, "attend_tflops": att_tflops,
         "dense_ms": dense_ms,
@@ -336,6 +338,73 @@ def run_gpu(args, w, rank, world):
     ctx.close()
 
 
+def run_sweep(args):
+    """Latency over sequence length (Llama-3-8B layer shape, 8k .. 512k): crisp_prefill and
+    crisp_dense per layer on the same seeded inputs, one JSON line per length, then the
+    estimated sparse/dense crossover length (log-log interpolation of the speedup)."""
+    import torch
+    import dynamic_sparse_prefill_gb300 as dsp
+    from workloads import get
+    from workloads.configs import SWEEP
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    pts = []
+    for name in SWEEP:
+        w = get(name)
+        g = make_inputs(w)
+        dev_t = lambda u16: torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).cuda()
+        q, k, v = dev_t(g["q"]), dev_t(g["k"]), dev_t(g["v"])
+        del g
+        o = torch.empty_like(q)
+        dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+        ctx = dsp.Context(dims)
+        cfg = dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy,
+                              k_min_tokens=w.k_min_tokens)
+
+        def timed(fn, reps):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        reps = 10 if w.n <= 65536 else 3
+        sel_ms = timed(lambda: ctx.select(dims, q, k, cfg), reps)
+        pre_ms = timed(lambda: ctx.prefill(dims, q, k, v, cfg, o), reps)
+        att_ms = timed(lambda: ctx.attend(dims, q, k, v, o), reps)
+        den_ms = timed(lambda: ctx.dense(dims, q, k, v, o), max(1, reps // 2))
+        if ctx.sync_status() != 0:
+            raise RuntimeError(f"device error in the sweep at {name}")
+        st = ctx.stats(dims)
+        nbk = w.n // B
+        line = {"sweep": True, "workload": name, "n": w.n, "prefill_ms": pre_ms,
+                "select_ms": sel_ms, "attend_ms": att_ms, "dense_ms": den_ms,
+                "speedup_vs_dense": den_ms / pre_ms,
+                "attend_tflops": algorithmic_flops(st["nnz"], st["rows"]) / (att_ms * 1e-3) / 1e12,
+                "dense_tflops": algorithmic_flops(w.hq * nbk * (nbk + 1) // 2, w.hq * nbk)
+                / (den_ms * 1e-3) / 1e12,
+                "density": st["nnz"] / (w.hq * nbk * (nbk + 1) / 2)}
+        print(json.dumps(line), flush=True)
+        pts.append((w.n, den_ms / pre_ms))
+        ctx.close()
+        del q, k, v, o
+        torch.cuda.empty_cache()
+    cross = None
+    for (n0, s0), (n1, s1) in zip(pts, pts[1:]):
+        if s0 < 1.0 <= s1:
+            f = (math.log(1.0) - math.log(s0)) / (math.log(s1) - math.log(s0))
+            cross = math.exp(math.log(n0) + f * (math.log(n1) - math.log(n0)))
+            break
+    if cross is None and pts and pts[0][1] >= 1.0:
+        cross = f"below {pts[0][0]}"
+    print(json.dumps({"sweep_summary": True, "crossover_tokens": cross,
+                      "speedups": {n: s for n, s in pts}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -347,7 +416,15 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0)
+    ap.add_argument("--vs-variant", default="none", choices=["none", "median", "gamma"],
+                    help="VS selection variant: median noise floor, or FlexPrefill's "
+                         "gamma-cumsum budget (the Abl.1 rule)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="latency sweep 8k..512k (one line per length), not the bench line")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     from workloads import get
     w = get(args.workload)
     world = int(os.environ.get("WORLD_SIZE", "1"))

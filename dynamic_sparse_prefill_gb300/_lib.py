@@ -18,6 +18,8 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "NO_MEMORY", 4: 
                 5: "TIMEOUT", 6: "DEVICE_ASSERT", 7: "NO_SELECTION"}
 FLAG_FORCE_VS = 0x1
 FLAG_FORCE_PE = 0x2
+FLAG_MEDIAN_FLOOR = 0x4
+FLAG_VS_GAMMA_CUMSUM = 0x8
 DEBUG_DROP_ARRIVE = 0x1
 
 # Every entry point include/crisp.h declares.

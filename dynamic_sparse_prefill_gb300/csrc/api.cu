@@ -47,6 +47,8 @@ crisp_status check_cfg(const crisp_cfg* c) {
   if (!(c->tau_proxy == c->tau_proxy)) return CRISP_ERR_INVALID_ARG;
   if ((c->flags & CRISP_FLAG_FORCE_VS) && (c->flags & CRISP_FLAG_FORCE_PE))
     return CRISP_ERR_INVALID_ARG;
+  if ((c->flags & CRISP_FLAG_MEDIAN_FLOOR) && (c->flags & CRISP_FLAG_VS_GAMMA_CUMSUM))
+    return CRISP_ERR_INVALID_ARG;
   return CRISP_OK;
 }
 

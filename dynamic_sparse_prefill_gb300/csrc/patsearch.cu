@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(256) proxy_pool_kernel(
 
 struct RouteArgs {
   int nb;
-  float inv_b, tau, alpha;
+  int n2;  // power of two >= nb (sort width)
+  float inv_b, tau, alpha, gamma;
   int kmin_blocks;
   uint32_t flags;
   const float* st_m;
@@ -412,14 +413,103 @@ __device__ void select_direction(const float* p, uint8_t* sel, int nb, float thr
   *out_k = k;
 }
 
+
+// Keys that sort ascending as (score descending, index ascending); scores are >= 0, so
+// their bit patterns order like the values.
+__device__ __forceinline__ uint64_t desc_key(float v, int idx) {
+  return (static_cast<uint64_t>(0xFFFFFFFFu - __float_as_uint(v)) << 32) |
+         static_cast<uint32_t>(idx);
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+  return __uint_as_float(0xFFFFFFFFu - static_cast<uint32_t>(k >> 32));
+}
+
+// Bitonic sort (ascending) of keys for p[lo .. lo+cnt) into keys[0 .. n2); the padding
+// keys sort last.  Whole block; ends synchronised.
+__device__ void sort_desc(const float* p, int lo, int cnt, uint64_t* keys, int n2) {
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    keys[i] = i < cnt ? desc_key(p[lo + i], lo + i) : ~0ull;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = keys[i], b = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Median of the non-anchor scores p[1 .. nb-2] (mean of the two middle values for an
+// even count); 0 when N_b <= 2.
+__device__ float median_floor(const float* p, int nb, uint64_t* keys, int n2) {
+  if (nb <= 2) return 0.f;
+  const int cnt = nb - 2;
+  sort_desc(p, 1, cnt, keys, n2);
+  const float hi = key_value(keys[(cnt - 1) / 2]);
+  const float lo = key_value(keys[cnt / 2]);
+  __syncthreads();
+  return 0.5f * (hi + lo);
+}
+
+// FlexPrefill-style budget: the smallest prefix of the scores sorted in descending
+// order (ties: lower index) whose fp64 running sum reaches gamma (all blocks if it never
+// does), padded to kmin; marks the chosen blocks in sel.
+__device__ void select_gamma_cumsum(const float* p, uint8_t* sel, int nb, float gamma, int kmin,
+                                    uint64_t* keys, int n2, double* part, int* first,
+                                    int* out_c, int* out_k) {
+  sort_desc(p, 0, nb, keys, n2);
+  const int per = (nb + blockDim.x - 1) / blockDim.x;
+  const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
+  double s = 0.0;
+  for (int i = b0; i < b1; ++i) s += static_cast<double>(key_value(keys[i]));
+  part[threadIdx.x] = s;
+  if (threadIdx.x == 0) *first = nb;
+  __syncthreads();
+  for (int off = 1; off < static_cast<int>(blockDim.x); off <<= 1) {
+    const double t = threadIdx.x >= static_cast<unsigned>(off) ? part[threadIdx.x - off] : 0.0;
+    __syncthreads();
+    part[threadIdx.x] += t;
+    __syncthreads();
+  }
+  double run = part[threadIdx.x] - s;
+  for (int i = b0; i < b1; ++i) {
+    run += static_cast<double>(key_value(keys[i]));
+    if (run >= static_cast<double>(gamma)) {
+      atomicMin(first, i + 1);
+      break;
+    }
+  }
+  __syncthreads();
+  const int c = *first;
+  const int k = min(max(c, kmin), nb);
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) sel[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < k; i += blockDim.x) sel[static_cast<uint32_t>(keys[i])] = 1;
+  __syncthreads();
+  *out_c = c;
+  *out_k = k;
+}
+
 __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a) {
-  extern __shared__ float sdyn[];
-  float* spv = sdyn;
-  float* sps = sdyn + a.nb;
-  uint8_t* ssv = reinterpret_cast<uint8_t*>(sps + a.nb);
-  uint8_t* sss = ssv + a.nb;
+  extern __shared__ uint64_t sdyn64[];
+  uint64_t* keys = sdyn64;                                  // [n2]
+  float* spv = reinterpret_cast<float*>(keys + a.n2);       // [nb]
+  float* sps = spv + a.nb;                                  // [nb]
+  uint8_t* ssv = reinterpret_cast<uint8_t*>(sps + a.nb);    // [nb]
+  uint8_t* sss = ssv + a.nb;                                // [nb]
   __shared__ int red[32];
   __shared__ float redf[32];
+  __shared__ double part[1024];
+  __shared__ int first;
   const int h = blockIdx.x;
   const int nb = a.nb;
   const size_t hb = static_cast<size_t>(h) * nb;
@@ -467,13 +557,25 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
     }
     return;
   }
-  // Noise floor mu_d = max(1 - p_d[0] - p_d[N_b-1], 0)/(N_b-2)  (Algorithm 3).
-  const float mu_v = nb > 2 ? fmaxf(1.f - spv[0] - spv[nb - 1], 0.f) / (nb - 2) : 0.f;
-  const float mu_s = nb > 2 ? fmaxf(1.f - sps[0] - sps[nb - 1], 0.f) / (nb - 2) : 0.f;
+  // Noise floor mu_d = max(1 - p_d[0] - p_d[N_b-1], 0)/(N_b-2)  (Algorithm 3), or the
+  // median of the non-anchor scores with CRISP_FLAG_MEDIAN_FLOOR.
+  float mu_v, mu_s;
+  if (a.flags & CRISP_FLAG_MEDIAN_FLOOR) {
+    mu_v = median_floor(spv, nb, keys, a.n2);
+    mu_s = median_floor(sps, nb, keys, a.n2);
+  } else {
+    mu_v = nb > 2 ? fmaxf(1.f - spv[0] - spv[nb - 1], 0.f) / (nb - 2) : 0.f;
+    mu_s = nb > 2 ? fmaxf(1.f - sps[0] - sps[nb - 1], 0.f) / (nb - 2) : 0.f;
+  }
   int cv, kv, cs, ks;
-  select_direction(spv, ssv, nb, a.alpha * mu_v, a.kmin_blocks, red, redf, &cv, &kv);
-  __syncthreads();
-  select_direction(sps, sss, nb, a.alpha * mu_s, a.kmin_blocks, red, redf, &cs, &ks);
+  if (a.flags & CRISP_FLAG_VS_GAMMA_CUMSUM) {
+    select_gamma_cumsum(spv, ssv, nb, a.gamma, a.kmin_blocks, keys, a.n2, part, &first, &cv, &kv);
+    select_gamma_cumsum(sps, sss, nb, a.gamma, a.kmin_blocks, keys, a.n2, part, &first, &cs, &ks);
+  } else {
+    select_direction(spv, ssv, nb, a.alpha * mu_v, a.kmin_blocks, red, redf, &cv, &kv);
+    __syncthreads();
+    select_direction(sps, sss, nb, a.alpha * mu_s, a.kmin_blocks, red, redf, &cs, &ks);
+  }
   __syncthreads();
   for (int J = threadIdx.x; J < nb; J += blockDim.x) {
     a.selv[hb + J] = ssv[J];
@@ -525,6 +627,9 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   r.inv_b = 1.f / kBlk;
   r.tau = cfg.tau_proxy;
   r.alpha = cfg.alpha;
+  r.gamma = cfg.gamma;
+  r.n2 = 1;
+  while (r.n2 < s.nb) r.n2 <<= 1;
   r.kmin_blocks = (cfg.k_min_tokens + kBlk - 1) / kBlk;
   r.flags = cfg.flags;
   r.st_m = w.st_m;
@@ -541,7 +646,8 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   r.counts = w.counts;
   r.selv = w.selv;
   r.sels = w.sels;
-  const size_t dyn = static_cast<size_t>(s.nb) * (2 * sizeof(float) + 2);
+  const size_t dyn = static_cast<size_t>(r.n2) * sizeof(uint64_t) +
+                    static_cast<size_t>(s.nb) * (2 * sizeof(float) + 2);
   route_vs_select_kernel<<<s.H, 1024, dyn, st>>>(r);
   return cudaGetLastError();
 }
@@ -551,8 +657,9 @@ cudaError_t init_patsearch_attributes() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kProxySmem));
   if (e != cudaSuccess) return e;
+  // nb <= 8192: 64 KB of sort keys + 80 KB of scores and flags (+ 8.4 KB static)
   return cudaFuncSetAttribute(route_vs_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              1 << 17);
+                              160 * 1024);
 }
 
 }  // namespace crisp

@@ -18,7 +18,9 @@
  *     uses key/value head h / (hq/hkv) of the same batch entry (GQA).
  *   - Supported shapes: d == 128, n a multiple of 128 with 128 <= n <= 1048576,
  *     hq % hkv == 0, batch*hq <= 65535.  Parameters: B == b == 128,
- *     1 <= w_sink, w_local <= 128, 0 < gamma <= 1, alpha >= 0, k_min_tokens >= 0.
+ *     1 <= w_sink, w_local <= 128, 0 < gamma <= 1, alpha >= 0, k_min_tokens >= 0;
+ *     CRISP_FLAG_FORCE_VS and CRISP_FLAG_FORCE_PE are exclusive, and so are
+ *     CRISP_FLAG_MEDIAN_FLOOR and CRISP_FLAG_VS_GAMMA_CUMSUM.
  *     Anything else returns CRISP_ERR_INVALID_ARG or CRISP_ERR_UNSUPPORTED before any
  *     work is queued.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute entry points
@@ -76,6 +78,11 @@ typedef struct {
 
 #define CRISP_FLAG_FORCE_VS 0x1u /* route every head VS (C_struct still computed) */
 #define CRISP_FLAG_FORCE_PE 0x2u /* route every head PE                          */
+/* VS variants ("Limitations" item 6, "Weaknesses" item 4; Table 5 ablation Abl.1): */
+#define CRISP_FLAG_MEDIAN_FLOOR 0x4u     /* mu_d = median of p_d[1..N_b-2] instead of the mean */
+#define CRISP_FLAG_VS_GAMMA_CUMSUM 0x8u  /* VS blocks by cumulative coverage >= gamma (largest
+                                            first, padded to k_min) instead of p_d > alpha*mu_d;
+                                            FlexPrefill's budget rule                          */
 
 /* Debug flags for crisp_set_debug. */
 #define CRISP_DEBUG_DROP_ARRIVE 0x1u /* attention: skip one barrier arrive in the first
@@ -125,7 +132,8 @@ typedef struct {
   uint8_t* route_vs;    /* [H]        1 = VS, 0 = PE                                  */
   float* c_struct;      /* [H]        C_struct                                       */
   float* mu;            /* [H][2]     mu_v, mu_s (VS heads; 0 for PE)                 */
-  int32_t* counts;      /* [H][4]     VS: c_v, c_s, k_v, k_s.
+  int32_t* counts;      /* [H][4]     VS: c_v, c_s, k_v, k_s (c_d = blocks above the floor,
+                                      or the gamma-cumsum cut size with CRISP_FLAG_VS_GAMMA_CUMSUM).
                                       PE: pairs kept by the gamma cut, rescued rows, 0, 0 */
   float* p_v;           /* [H][N_b]   pooled vertical score (all heads)               */
   float* p_s;           /* [H][N_b]   pooled slash score (all heads)                  */

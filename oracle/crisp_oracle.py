@@ -116,6 +116,20 @@ def noise_floor(p: np.ndarray) -> float:
     return r / (nb - 2)
 
 
+def noise_floor_median(p: np.ndarray) -> float:
+    """Variant floor: the median of the non-anchor block scores p_d[1..N_b-2] instead of
+    their mean ("Limitations" item 6 and "Weaknesses" item 4: the mean floor can be lifted
+    by one dominant block; the median variant changes accuracy by about 0.7 pp).
+
+    Reading: the median of an even count is the mean of the two middle values; with
+    N_b <= 2 there is no non-anchor block and mu = 0, as for the mean floor.
+    """
+    nb = p.shape[0]
+    if nb <= 2:
+        return 0.0
+    return float(np.median(p[1:nb - 1]))
+
+
 def topk_desc(p: np.ndarray, k: int) -> np.ndarray:
     """Indices of the k largest values, ties broken toward the lower index; sorted."""
     order = np.lexsort((np.arange(p.shape[0]), -p))
@@ -135,21 +149,42 @@ def select_above_floor(p: np.ndarray, alpha: float, mu: float, kmin_blocks: int)
     return topk_desc(p, kd), c, kd
 
 
+def select_gamma_cumsum(p: np.ndarray, gamma: float, kmin_blocks: int):
+    """FlexPrefill's VS budget as the page describes it ("Prerequisites", cumulative
+    coverage; "Novelty" and Table 5, ablation Abl.1 = C_struct routing with this rule):
+    the smallest set of blocks, largest first, whose scores reach gamma, padded to the
+    minimum budget k_min.  Returns (sorted block indices, cut size, k_d)."""
+    nb = p.shape[0]
+    cut = gamma_cut(p, gamma).size
+    kd = min(max(cut, kmin_blocks), nb)
+    return topk_desc(p, kd), cut, kd
+
+
 def kmin_blocks(k_min_tokens: int, B: int) -> int:
     """k_min of 1024 tokens is 8 blocks of 128 per direction [Steps]."""
     return -(-k_min_tokens // B)
 
 
-def vs_index(a_hat: np.ndarray, B: int, alpha: float, k_min_tokens: int) -> dict:
-    """Algorithm 3: vertical and slash scores, pooled, floored and selected."""
+def vs_index(a_hat: np.ndarray, B: int, alpha: float, k_min_tokens: int, floor: str = "mean",
+             vs_rule: str = "floor", gamma: float = 0.95) -> dict:
+    """Algorithm 3: vertical and slash scores, pooled, floored and selected.
+
+    floor="median" uses noise_floor_median; vs_rule="gamma" replaces the floor rule by the
+    gamma-cumsum budget (select_gamma_cumsum), mu is then still reported.
+    """
     a_v = vertical_score(a_hat)
     a_s = slash_score(a_hat)
     p_v = block_pool(a_v, B)
     p_s = block_pool(a_s, B)
     kmb = kmin_blocks(k_min_tokens, B)
-    mu_v, mu_s = noise_floor(p_v), noise_floor(p_s)
-    S_v, c_v, k_v = select_above_floor(p_v, alpha, mu_v, kmb)
-    S_s, c_s, k_s = select_above_floor(p_s, alpha, mu_s, kmb)
+    fl = noise_floor_median if floor == "median" else noise_floor
+    mu_v, mu_s = fl(p_v), fl(p_s)
+    if vs_rule == "gamma":
+        S_v, c_v, k_v = select_gamma_cumsum(p_v, gamma, kmb)
+        S_s, c_s, k_s = select_gamma_cumsum(p_s, gamma, kmb)
+    else:
+        S_v, c_v, k_v = select_above_floor(p_v, alpha, mu_v, kmb)
+        S_s, c_s, k_s = select_above_floor(p_s, alpha, mu_s, kmb)
     return dict(a_v=a_v, a_s=a_s, p_v=p_v, p_s=p_s, mu_v=mu_v, mu_s=mu_s,
                 S_v=S_v, S_s=S_s, c_v=c_v, c_s=c_s, k_v=k_v, k_s=k_s, kmin_blocks=kmb)
 
@@ -257,10 +292,12 @@ def block_sparse_attention(q, k, v, mask: np.ndarray, B: int, blocks=None) -> np
 # Algorithm 1 per head [Steps], [Alg1 under "Figures and tables"]
 # --------------------------------------------------------------------------------------
 def crisp_select_head(q, k, B=128, b=128, w_sink=128, w_local=128, tau_proxy=0.2,
-                      alpha=1.0, gamma=0.95, k_min_tokens=1024, force=None) -> dict:
+                      alpha=1.0, gamma=0.95, k_min_tokens=1024, force=None, floor="mean",
+                      vs_rule="floor") -> dict:
     """PatSearch -> VSIndex or PEIndex for one query head (fp64 inputs [n, d]).
 
     force: None, "vs" or "pe" overrides the route (the C_struct value is still computed).
+    floor / vs_rule: the median-floor and gamma-cumsum VS variants (see vs_index).
     """
     n = k.shape[0]
     nb = n // B
@@ -270,7 +307,7 @@ def crisp_select_head(q, k, B=128, b=128, w_sink=128, w_local=128, tau_proxy=0.2
     is_vs = route_is_vs(c, tau_proxy) if force is None else (force == "vs")
     res = dict(c_struct=c, route_vs=is_vs, n_blocks=nb)
     if is_vs:
-        vs = vs_index(a_hat, B, alpha, k_min_tokens)
+        vs = vs_index(a_hat, B, alpha, k_min_tokens, floor=floor, vs_rule=vs_rule, gamma=gamma)
         res.update(vs)
         res["mask"] = vs_block_mask(vs["S_v"], vs["S_s"], nb)
     else:
@@ -289,7 +326,8 @@ def crisp_head(q, k, v, blocks=None, **params) -> dict:
 def workload_params(w) -> dict:
     """The method parameters of a workload description (B, b, windows, tau, alpha, ...)."""
     return dict(B=w.B, b=w.b, w_sink=w.w_sink, w_local=w.w_local, tau_proxy=w.tau_proxy,
-                alpha=w.alpha, gamma=w.gamma, k_min_tokens=w.k_min_tokens)
+                alpha=w.alpha, gamma=w.gamma, k_min_tokens=w.k_min_tokens,
+                floor=getattr(w, "vs_floor", "mean"), vs_rule=getattr(w, "vs_rule", "floor"))
 
 
 def mass_cliff_epsilon(n: int, k: int, delta: float) -> float:

@@ -111,13 +111,15 @@ def compare_selection(w, sel, osel, heads=None):
                 gp = sel["p_" + d][h]
                 err = np.abs(gp - p) / (np.abs(p) + 1e-6)
                 rep["max_p_err"] = max(rep["max_p_err"], float(err.max()))
+                gamma_rule = getattr(w, "vs_rule", "floor") == "gamma"
                 thr = w.alpha * o["mu_" + d]
                 osel_set = np.zeros(nb, bool)
                 osel_set[o["S_" + d]] = True
                 diff = np.nonzero(osel_set != sel[key][h].astype(bool))[0]
-                kth = _kth_largest(p, o["k_" + d]) if o["k_" + d] > o["c_" + d] else None
+                kth = _kth_largest(p, o["k_" + d]) if (gamma_rule or o["k_" + d] > o["c_" + d]) \
+                    else None
                 for J in diff:
-                    near = abs(p[J] - thr) <= TOL_REL * thr
+                    near = (not gamma_rule) and abs(p[J] - thr) <= TOL_REL * thr
                     if kth is not None:
                         near |= abs(p[J] - kth) <= TOL_REL * kth
                     assert near, (f"head {h} dir {d}: block {J} differs (p={p[J]:.6g}, "

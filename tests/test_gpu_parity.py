@@ -26,10 +26,14 @@ def dsp():
     return d
 
 
-def _cfg(dsp, w, **kw):
+def _cfg(dsp, w, flags=0):
+    if w.vs_floor == "median":
+        flags |= dsp.FLAG_MEDIAN_FLOOR
+    if w.vs_rule == "gamma":
+        flags |= dsp.FLAG_VS_GAMMA_CUMSUM
     return dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy,
                            k_min_tokens=w.k_min_tokens, w_sink=w.w_sink, w_local=w.w_local,
-                           **kw)
+                           flags=flags)
 
 
 def _rows(blocks, B=128):
@@ -250,3 +254,23 @@ def test_llama_n512k_sampled_and_dense(dsp):
         ref = O.block_sparse_attention(qh, kh, vh, full, 128, bl)
         compare_outputs(got[i][_rows(bl)], ref, f"dense 512k head {h}")
     ctx.close()
+
+
+@pytest.mark.parametrize("name,sample", [("llama8b_n8k", None), ("llama8b_n16k", None),
+                                         ("llama8b_n64k", (8, 16)), ("llama8b_n256k", (8, 16))])
+def test_sweep_lengths(dsp, name, sample):
+    """The other lengths of the latency sweep hold the same parity bar."""
+    w = get(name)
+    rep, _, _ = run_parity(dsp, w, generate(w), sample=sample, seed=3)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("name", ["tiny_n4k", "llama8b_n32k"])
+@pytest.mark.parametrize("variant", [dict(vs_floor="median"), dict(vs_rule="gamma")])
+def test_vs_variants(dsp, name, variant):
+    """Median noise floor and FlexPrefill's gamma-cumsum VS budget (the Abl.1 rule) hold
+    the same parity bar as the page's rule."""
+    w = get(name).with_params(**variant)
+    rep, sel, osel = run_parity(dsp, w, generate(w), sample=None if name == "tiny_n4k" else (8, 8),
+                                seed=5)
+    print(name, variant, rep)

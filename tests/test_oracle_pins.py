@@ -325,3 +325,34 @@ def test_planted_tiny_routes_and_end_to_end_bruteforce():
             e = np.exp(logits - logits.max(axis=1, keepdims=True))
             ref = (e / e.sum(axis=1, keepdims=True)) @ v
             np.testing.assert_allclose(res["out"][bi * B:(bi + 1) * B], ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- VS variants (NEXT rows)
+def test_vs_variants_worked_example():
+    """Median noise floor and the gamma-cumsum VS budget against a hand-worked example."""
+    fx = json.load(open(os.path.join(GOLD, "vs_variants_worked.json")))
+    p = np.array(fx["p"])
+    assert abs(O.noise_floor_median(p) - fx["median"]) < 1e-15
+    assert abs(O.noise_floor(p) - fx["mean"]) < 1e-15
+    for case in fx["median_floor_cases"]:
+        S, _, _ = O.select_above_floor(p, case["alpha"], O.noise_floor_median(p), case["kmin_blocks"])
+        assert S.tolist() == case["selected"]
+    for case in fx["gamma_cases"]:
+        S, cut, kd = O.select_gamma_cumsum(p, case["gamma"], case["kmin_blocks"])
+        assert cut == case["cut"] and S.tolist() == case["selected"]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_median_floor_bruteforce(seed):
+    """The median floor is the middle order statistic of the non-anchor scores (counted
+    directly): as many scores lie at or below it as at or above it."""
+    rng = np.random.default_rng(200 + seed)
+    for nb in (3, 4, 9, 10, 33):
+        p = rng.dirichlet(np.ones(nb))
+        mid = O.noise_floor_median(p)
+        inner = p[1:nb - 1]
+        assert np.count_nonzero(inner <= mid) >= (nb - 2 + 1) // 2
+        assert np.count_nonzero(inner >= mid) >= (nb - 2 + 1) // 2
+        if (nb - 2) % 2 == 1:
+            assert mid in inner
+    assert O.noise_floor_median(np.array([0.4, 0.6])) == 0.0

@@ -40,6 +40,8 @@ class Workload:
     tau_proxy: float = 0.2
     alpha: float = 1.0
     gamma: float = 0.95
+    vs_floor: str = "mean"      # "mean" (the page's rule) or "median" (variant)
+    vs_rule: str = "floor"      # "floor" (alpha * mu) or "gamma" (cumulative coverage variant)
 
     @property
     def group(self) -> int:
@@ -76,11 +78,23 @@ WORKLOADS = {
     "qwen7b_n128k": Workload("qwen7b_n128k", n=131072, hq=28, hkv=4, seed=1003,
                              sink_scale=5.0, needles=("uniform", 2, 16),
                              pe_heads=_one_pe_per_group(28, 4)),
+    # Llama-3-8B layer shape at the other lengths of the latency sweep (8k .. 256k).
+    **{f"llama8b_n{n // 1024}k": Workload(f"llama8b_n{n // 1024}k", n=n, hq=32, hkv=8, seed=1100 + i,
+                                          sink_scale=4.0, needles=("uniform", 2, 16),
+                                          pe_heads=_one_pe_per_group(32, 8))
+       for i, n in enumerate((8192, 16384, 65536, 262144))},
     # Llama-3-8B layer shape at 512k tokens, 16 needle blocks per VS head.
     "llama8b_n512k": Workload("llama8b_n512k", n=524288, hq=32, hkv=8, seed=1004,
                               sink_scale=4.0, needles=("fixed", 16),
                               pe_heads=_one_pe_per_group(32, 8)),
 }
+
+
+# The latency sweep over sequence length (Llama-3-8B layer shape): the page's latency
+# table spans 64k-512k and its limitations section places the sparse/dense crossover
+# between 8k and 64k.
+SWEEP = ("llama8b_n8k", "llama8b_n16k", "llama8b_n32k", "llama8b_n64k", "llama8b_n128k_a1",
+         "llama8b_n256k", "llama8b_n512k")
 
 
 def get(name: str) -> Workload:
