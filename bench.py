@@ -405,6 +405,54 @@ def run_sweep(args):
                       "speedups": {n: s for n, s in pts}}), flush=True)
 
 
+def run_jsd(args):
+    """Routing-signal comparison: FlexPrefill's JSD (crisp_jsd) against C_struct on the
+    same heads -- cost of the extra pooled estimate and KL passes, and agreement of the
+    two routes.  One JSON line per workload."""
+    import torch
+    import dynamic_sparse_prefill_gb300 as dsp
+    from workloads import get
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    for name in ("llama8b_n32k", "llama8b_n128k_a1", "qwen7b_n128k", "llama8b_n512k"):
+        w = get(name)
+        g = make_inputs(w)
+        dev_t = lambda u16: torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).cuda()
+        q, k = dev_t(g["q"]), dev_t(g["k"])
+        del g
+        dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+        ctx = dsp.Context(dims)
+        cfg = dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy)
+        d_js = torch.zeros(w.hq, dtype=torch.float32, device="cuda")
+        rt = torch.zeros(w.hq, dtype=torch.uint8, device="cuda")
+        ctx.select(dims, q, k, cfg)
+        ctx.jsd(dims, q, k, args.tau_jsd, d_js, rt)
+        torch.cuda.synchronize()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        reps = 5
+        e[0].record(stream)
+        for _ in range(reps):
+            ctx.select(dims, q, k, cfg)
+        e[1].record(stream)
+        for _ in range(reps):
+            ctx.jsd(dims, q, k, args.tau_jsd, d_js, rt)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        if ctx.sync_status() != 0:
+            raise RuntimeError("device error in the JSD comparison")
+        sel = ctx.selection_get(dims, with_csr=False)
+        routes = rt.cpu().numpy()
+        agree = int((routes == sel["route_vs"]).sum())
+        print(json.dumps({"jsd": True, "workload": name, "n": w.n, "tau_jsd": args.tau_jsd,
+                          "select_ms": e[0].elapsed_time(e[1]) / reps,
+                          "jsd_extra_ms": e[1].elapsed_time(e[2]) / reps,
+                          "route_agreement": agree / w.hq,
+                          "d_js": [round(float(x), 5) for x in d_js.cpu().numpy()]}), flush=True)
+        ctx.close()
+        del q, k
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,11 +467,17 @@ def main():
     ap.add_argument("--vs-variant", default="none", choices=["none", "median", "gamma"],
                     help="VS selection variant: median noise floor, or FlexPrefill's "
                          "gamma-cumsum budget (the Abl.1 rule)")
+    ap.add_argument("--jsd", action="store_true",
+                    help="JSD vs C_struct routing comparison (one line per workload)")
+    ap.add_argument("--tau-jsd", type=float, default=0.1)
     ap.add_argument("--sweep", action="store_true",
                     help="latency sweep 8k..512k (one line per length), not the bench line")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.jsd:
+        run_jsd(args)
         return
     from workloads import get
     w = get(args.workload)

@@ -26,7 +26,7 @@ DEBUG_DROP_ARRIVE = 0x1
 EXPORTED = ["crisp_cfg_default", "crisp_create", "crisp_destroy", "crisp_select", "crisp_attend",
             "crisp_prefill", "crisp_dense", "crisp_selection_get", "crisp_selection_set",
             "crisp_selection_stats", "crisp_sync_status", "crisp_set_debug",
-            "crisp_status_string", "crisp_last_error", "crisp_route_static"]
+            "crisp_status_string", "crisp_last_error", "crisp_route_static", "crisp_jsd"]
 
 
 class Dims(ctypes.Structure):
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "crisp_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "crisp_last_error": (ctypes.c_char_p, [P]),
         "crisp_route_static": (ctypes.c_int, [DP, P, P, CP, P, P, P, P]),
+        "crisp_jsd": (ctypes.c_int, [P, DP, P, P, ctypes.c_float, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -166,6 +167,12 @@ class Context:
     def dense(self, dims, q, k, v, o, stream=None):
         self._check(self._lib.crisp_dense(self._h, ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v),
                                           _ptr(o), _stream(stream)), "crisp_dense")
+
+    def jsd(self, dims, q, k, tau_jsd, d_js, route_vs, stream=None):
+        """FlexPrefill's JSD routing signal for the current selection (device outputs)."""
+        self._check(self._lib.crisp_jsd(self._h, ctypes.byref(dims), _ptr(q), _ptr(k),
+                                        ctypes.c_float(tau_jsd), _ptr(d_js), _ptr(route_vs),
+                                        _stream(stream)), "crisp_jsd")
 
     def sync_status(self, stream=None) -> int:
         return self._lib.crisp_sync_status(self._h, _stream(stream))

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcrisp.so")
-SOURCES = ["api.cu", "patsearch.cu", "pe_index.cu", "csr.cu", "attention.cu"]
+SOURCES = ["api.cu", "patsearch.cu", "pe_index.cu", "csr.cu", "attention.cu", "jsd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -263,12 +263,14 @@ crisp_status crisp_select(crisp_ctx ctx, const crisp_dims* dims, const void* Q, 
   if ((st = make_map(ctx, &tmQ, Q, static_cast<int64_t>(s.H) * s.n)) != CRISP_OK) return st;
   if ((st = make_map(ctx, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
   ctx->has_sel = false;
+  ctx->has_patsearch = false;
   if ((st = launched(ctx, launch_patsearch(ctx, s, *cfg, tmQ, tmK, cs), "patsearch")) != CRISP_OK)
     return st;
   if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, cs), "pe_index")) != CRISP_OK)
     return st;
   if ((st = launched(ctx, launch_build_csr(ctx, s, cs), "build_csr")) != CRISP_OK) return st;
   ctx->has_sel = true;
+  ctx->has_patsearch = true;
   ctx->sel_dims = *dims;
   return CRISP_OK;
 }
@@ -375,8 +377,23 @@ crisp_status crisp_selection_set(crisp_ctx ctx, const crisp_dims* dims, void* st
                      "upload col")) != CRISP_OK)
     return st;
   ctx->has_sel = true;
+  ctx->has_patsearch = false;
   ctx->sel_dims = *dims;
   return CRISP_OK;
+}
+
+crisp_status crisp_jsd(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                       float tau_jsd, float* d_js, uint8_t* route_vs, void* stream) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if (!Q || !K || !d_js || !route_vs || !aligned16(Q) || !aligned16(K) || !(tau_jsd == tau_jsd))
+    return CRISP_ERR_INVALID_ARG;
+  if (!ctx->has_sel || !ctx->has_patsearch || !same_dims(ctx->sel_dims, *dims))
+    return CRISP_ERR_NO_SELECTION;
+  const Shape s = make_shape(*dims);
+  return launched(ctx,
+                  launch_jsd(ctx, s, Q, K, tau_jsd, d_js, route_vs, static_cast<cudaStream_t>(stream)),
+                  "jsd");
 }
 
 crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* stream,

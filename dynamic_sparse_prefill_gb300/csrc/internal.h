@@ -83,6 +83,7 @@ struct crisp_ctx_s {
   crisp::Workspace ws;
   crisp::EncodeTiledFn encode = nullptr;
   bool has_sel = false;
+  bool has_patsearch = false;  // workspace p_v belongs to the current selection
   crisp_dims sel_dims{};
   uint32_t debug_flags = 0;
   uint64_t timeout_ns = 1000000000ull;
@@ -102,6 +103,7 @@ cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st);
 cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& tmQ,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, void* O, bool dense,
                              cudaStream_t st);
-cudaError_t init_kernel_attributes();
+cudaError_t launch_jsd(crisp_ctx ctx, const Shape& s, const void* Q, const void* K, float tau,
+                       float* d_js, uint8_t* route, cudaStream_t st);
 
 }  // namespace crisp

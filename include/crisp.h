@@ -166,6 +166,19 @@ typedef struct {
 crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* stream,
                                    crisp_stats* out);
 
+/* Diagnostic: FlexPrefill's JSD routing signal, which CRISP's C_struct replaces
+ * ("Prerequisites", JSD; "Motivation").  For each query head, D_JS = 1/2 KL(a_hat || m) +
+ * 1/2 KL(a_bar || m), m = (a_hat + a_bar)/2, where a_hat is the pooled proxy attention
+ * p_v of the preceding crisp_select on the same Q/K (the "softmax, then average"
+ * distribution over key blocks) and a_bar is the softmax over key blocks of
+ * (mean of the last 128 queries) . (block mean of the keys) / sqrt(d) ("pool, then
+ * softmax").  Writes, in caller-owned device memory, d_js[H] (float, nats) and
+ * route_vs[H] (1 iff D_JS >= tau_jsd; the pages give no value for tau_jsd).  Returns
+ * CRISP_ERR_NO_SELECTION unless the context's last call was crisp_select / crisp_prefill
+ * with these dims.  Enqueues work on `stream` only. */
+crisp_status crisp_jsd(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
+                       float tau_jsd, float* d_js, uint8_t* route_vs, void* stream);
+
 /* Synchronise `stream`, then report and clear the device error word: CRISP_OK,
  * CRISP_ERR_TIMEOUT or CRISP_ERR_DEVICE_ASSERT, or CRISP_ERR_CUDA if the stream itself
  * reports a CUDA error. */

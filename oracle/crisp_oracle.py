@@ -330,6 +330,39 @@ def workload_params(w) -> dict:
                 floor=getattr(w, "vs_floor", "mean"), vs_rule=getattr(w, "vs_rule", "floor"))
 
 
+def kl_divergence(x: np.ndarray, y: np.ndarray) -> float:
+    """KL(x || y) = sum x log(x / y) in nats, with 0 log 0 = 0."""
+    nz = x > 0
+    return float(np.sum(x[nz] * np.log(x[nz] / y[nz])))
+
+
+def js_divergence(x: np.ndarray, y: np.ndarray) -> float:
+    """D_JS = 1/2 KL(x || m) + 1/2 KL(y || m), m = (x + y)/2  ("Prerequisites", JSD)."""
+    m = 0.5 * (x + y)
+    return 0.5 * kl_divergence(x, m) + 0.5 * kl_divergence(y, m)
+
+
+def pooled_estimate(q: np.ndarray, k: np.ndarray, B: int, b: int) -> np.ndarray:
+    """a_bar, the "pool first, then softmax" distribution over key blocks ("Prerequisites",
+    JSD): the mean of the last b queries against the block means of the keys, softmax over
+    the N_b blocks.  Reading: the pooled query stands for the last query block, which sees
+    every key block; the logits are scaled by 1/sqrt(d) like the attention's."""
+    n, d = k.shape
+    qbar = q[n - b:].mean(axis=0)
+    logits = block_mean(k, B) @ qbar / math.sqrt(d)
+    return _softmax_rows(logits[None, :])[0]
+
+
+def jsd_route(q: np.ndarray, k: np.ndarray, B: int, b: int, tau_jsd: float) -> dict:
+    """FlexPrefill's JSD routing, the signal C_struct replaces ("Prerequisites", JSD;
+    "Motivation"): a_hat = the proxy attention averaged over its b queries and pooled by
+    key block (p_v), a_bar = pooled_estimate; VS iff D_JS(a_hat, a_bar) >= tau_jsd."""
+    p_v = block_pool(vertical_score(proxy_attention(q, k, b)), B)
+    a_bar = pooled_estimate(q, k, B, b)
+    dj = js_divergence(p_v, a_bar)
+    return dict(d_js=dj, route_vs=bool(dj >= tau_jsd), a_hat=p_v, a_bar=a_bar)
+
+
 def mass_cliff_epsilon(n: int, k: int, delta: float) -> float:
     """Background-token mass of one softmax row with k signal logits delta and n-k zero
     logits: e^-delta / (k + (n-k) e^-delta)  [Core] innovation 2."""

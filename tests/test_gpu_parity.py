@@ -274,3 +274,39 @@ def test_vs_variants(dsp, name, variant):
     rep, sel, osel = run_parity(dsp, w, generate(w), sample=None if name == "tiny_n4k" else (8, 8),
                                 seed=5)
     print(name, variant, rep)
+
+
+@pytest.mark.parametrize("name", ["tiny_n4k", "llama8b_n32k", "qwen7b_n128k"])
+def test_jsd_routing_diagnostic(dsp, name):
+    """crisp_jsd (FlexPrefill's JSD signal) against the oracle: D_JS per head within
+    1e-4 + 1e-3 relative, JSD routes equal except within 1e-3 relative of tau_jsd."""
+    from oracle import crisp_oracle as O
+    w = get(name)
+    g = generate(w)
+    q, k = to_device(g["q"]), to_device(g["k"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    ctx.select(dims, q, k, _cfg(dsp, w))
+    tau = 0.1
+    d_js = torch.zeros(w.hq, dtype=torch.float32, device="cuda")
+    route = torch.zeros(w.hq, dtype=torch.uint8, device="cuda")
+    ctx.jsd(dims, q, k, tau, d_js, route)
+    assert ctx.sync_status() == 0
+    sel = ctx.selection_get(dims, with_csr=False)
+    dj, rt = d_js.cpu().numpy(), route.cpu().numpy()
+    agree = 0
+    for h in range(w.hq):
+        qh = O.bf16_bits_to_f64(g["q"][h])
+        kh = O.bf16_bits_to_f64(g["k"][h // w.group])
+        ref = O.jsd_route(qh, kh, w.B, w.b, tau)
+        assert abs(dj[h] - ref["d_js"]) <= 1e-4 + 1e-3 * ref["d_js"], (h, dj[h], ref["d_js"])
+        if bool(rt[h]) != ref["route_vs"]:
+            assert abs(ref["d_js"] - tau) <= 1e-3 * tau
+        agree += int(bool(rt[h]) == bool(sel["route_vs"][h]))
+    print(name, "JSD/C_struct route agreement", agree, "/", w.hq, "D_JS", np.round(dj, 4).tolist())
+    with pytest.raises(dsp.CrispError):   # p_v must come from crisp_select, not selection_set
+        nb = w.n_blocks
+        rp = np.arange(w.hq * nb + 1, dtype=np.int64)
+        ctx.selection_set(dims, rp, np.tile(np.arange(nb, dtype=np.int32), w.hq))
+        ctx.jsd(dims, q, k, tau, d_js, route)
+    ctx.close()

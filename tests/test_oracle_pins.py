@@ -356,3 +356,35 @@ def test_median_floor_bruteforce(seed):
         if (nb - 2) % 2 == 1:
             assert mid in inner
     assert O.noise_floor_median(np.array([0.4, 0.6])) == 0.0
+
+
+# ---------------------------------------------------------------- JSD routing (NEXT row)
+def test_js_divergence_closed_forms():
+    """D_JS = 0 for equal distributions; ln 2 for disjoint supports; a two-point closed
+    form for x = (1, 0), y = (1/2, 1/2): 1/2 ln(4/3) + 1/4 ln(2/3) + 1/4 ln 2."""
+    x = np.array([0.2, 0.3, 0.5])
+    assert abs(O.js_divergence(x, x)) < 1e-16
+    assert abs(O.js_divergence(np.array([1.0, 0, 0, 0]), np.array([0, 0, 0.5, 0.5])) - math.log(2)) < 1e-15
+    ref = 0.5 * math.log(4 / 3) + 0.25 * math.log(2 / 3) + 0.25 * math.log(2)
+    assert abs(O.js_divergence(np.array([1.0, 0.0]), np.array([0.5, 0.5])) - ref) < 1e-15
+    rng = np.random.default_rng(9)
+    for _ in range(5):
+        a, b = rng.dirichlet(np.ones(7)), rng.dirichlet(np.ones(7))
+        dj = O.js_divergence(a, b)
+        assert 0 <= dj <= math.log(2) and abs(dj - O.js_divergence(b, a)) < 1e-15
+
+
+def test_pooled_estimate_special_cases():
+    """Q = 0 gives a uniform a_bar; keys constant within each block and a query equal to
+    the block-J key give the softmax of the block dot products (closed form)."""
+    n, d, B, b = 1024, 8, 128, 128
+    k = np.random.default_rng(4).standard_normal((n, d))
+    np.testing.assert_allclose(O.pooled_estimate(np.zeros((n, d)), k, B, b), 1.0 / (n // B),
+                               rtol=1e-15)
+    nb = n // B
+    kb = np.random.default_rng(5).standard_normal((nb, d))
+    kc = np.repeat(kb, B, axis=0)
+    q = np.tile(kb[3], (n, 1))
+    z = kb @ kb[3] / math.sqrt(d)
+    ref = np.exp(z - z.max()) / np.exp(z - z.max()).sum()
+    np.testing.assert_allclose(O.pooled_estimate(q, kc, B, b), ref, rtol=1e-13)
