@@ -44,6 +44,26 @@ def algorithmic_flops(nnz: int, rows: int) -> float:
     return 4.0 * B * B * D * (nnz - rows) + 2.0 * D * B * (B + 1) * rows
 
 
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it
+    was taken on this workload with the current kernel source; else None."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", f"attention_kernel_{workload}_traffic.md")
+    src = os.path.join(ROOT, "dynamic_sparse_prefill_gb300", "csrc", "attention.cu")
+    if not os.path.exists(prof):
+        return None
+    text = open(prof).read()
+    m = re.search(r"source_sha256: ([0-9a-f]{64})", text)
+    rd = re.search(r"dram_bytes_read: (\d+)", text)
+    wr = re.search(r"dram_bytes_write: (\d+)", text)
+    if not (m and rd and wr):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m.group(1):
+        return None
+    return int(rd.group(1)) + int(wr.group(1))
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -199,9 +219,35 @@ def run_reference(args, w, rank, world):
 def workload_config(w):
     return {"workload": w.name, "n": w.n, "hq": w.hq, "hkv": w.hkv, "d": w.d, "batch": w.batch,
             "alpha": w.alpha, "gamma": w.gamma, "tau_proxy": w.tau_proxy, "B": w.B,
-            "k_min_tokens": w.k_min_tokens,
-            "l2": "inputs larger than L2 (Q alone is %.1f GB); no flush" %
-                  (w.hq * w.n * w.d * 2 / 1e9)}
+            "k_min_tokens": w.k_min_tokens, "l2": l2_note(w)}
+
+
+L2_BYTES = 129e6
+
+
+def l2_note(w) -> str:
+    q_bytes = w.batch * w.hq * w.n * w.d * 2
+    if q_bytes > L2_BYTES:
+        return "inputs larger than L2 (Q alone is %.2f GB); no flush" % (q_bytes / 1e9)
+    return "inputs smaller than L2 (Q is %.1f MB): timings include L2 reuse" % (q_bytes / 1e6)
+
+
+def max_over_ranks(value: float) -> float:
+    """Max of a per-rank number over all ranks (the slowest replica sets the step time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(ms_per_step: float, world: int) -> float:
+    """ms per layer of the whole job: `world` replicas each process one layer per step."""
+    return ms_per_step / world
 
 
 def run_gpu(args, w, rank, world):
@@ -252,15 +298,11 @@ def run_gpu(args, w, rank, world):
         dist.barrier()
     if ctx.sync_status() != 0:
         raise RuntimeError("device error during the timed region")
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
     sel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms_per_step = total_ms / args.steps
-    value = ms_per_step / world  # replicas: one layer per rank per step
+    value = replica_value(ms_per_step, world)
 
     # dense causal attention on the same inputs (the speedup denominator)
     dense_ms = None
@@ -324,7 +366,8 @@ def run_gpu(args, w, rank, world):
                       "pe_rescued_rows": stats["pe_rescued"], "max_row": stats["max_row"]},
         "roofline": {"kernel": "attention_kernel", "bound": "tensor", "achieved": att_tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": att_tflops / peak,
-                     "peak_kind": f"bf16 sustained, {peak_kind}", "traffic": None,
+                     "peak_kind": f"bf16 sustained, {peak_kind}",
+                     "traffic": recorded_traffic(w.name),
                      "algorithmic_flops_per_launch": flops},
         "gpu_launches": LAUNCHES_PER_PREFILL * args.steps,
         "e2e": {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -8,8 +8,8 @@
 // block K <= I selected this is dense causal attention, the speedup denominator.
 //
 // Persistent kernel: one CTA per SM walks work items (query head h, query block I) in
-// a static round-robin over an order with the longest rows first and the heads of a
-// GQA group adjacent.  Ten warps:
+// serpentine waves over an order that keeps each KV head's rows together, longest first
+// (see get_item).  Ten warps:
 //   warps 0-3  softmax of "tile 0": the even-numbered key blocks of the item's list;
 //   warps 4-7  softmax of "tile 1": the odd-numbered key blocks;
 //   warp 8     TMA producer of the item's Q tile and K_j (3-slot ring);
@@ -153,13 +153,25 @@ struct Item {
   int64_t beg;
 };
 
-__device__ __forceinline__ Item get_item(const AttnArgs& a, int k) {
+// Work item k of a CTA's round-robin sequence (k = blockIdx.x + i * G).  Items are taken
+// in waves of G consecutive entries of the order; odd waves are walked in reverse
+// (serpentine), so each CTA's total work stays balanced and the CTAs of a wave start and
+// advance together over the same key blocks -- the order keeps one KV head's rows
+// together, so those blocks are fetched from DRAM once per wave and served from L2.
+// Dense order: KV head major, then query block descending, then the group's q-heads.
+__device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G) {
+  const int m = k / G, pos = k % G;
+  const int base = m * G;
+  const int wsize = min(G, a.num_items - base);
+  const int ke = (m & 1) ? base + wsize - 1 - pos : k;
   Item it;
   if (a.dense) {
-    it.h = k % a.H;
-    it.I = a.nb - 1 - k / a.H;
+    const int per_kv = a.group * a.nb;
+    const int hk_all = ke / per_kv, r = ke % per_kv;
+    it.I = a.nb - 1 - r / a.group;
+    it.h = (hk_all / a.hkv) * a.hq + (hk_all % a.hkv) * a.group + r % a.group;
   } else {
-    const int row = a.order[k];
+    const int row = a.order[ke];
     it.h = row / a.nb;
     it.I = row % a.nb;
   }
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gk = 0, item_idx = 0, q_loads = 0;
       bool ok = true;
       for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
-        const Item it = get_item(a, k);
+        const Item it = get_item(a, k, gridDim.x);
         if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) {
           ok = false;
           break;
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gv = 0;
       bool ok = true;
       for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x) {
-        const Item it = get_item(a, k);
+        const Item it = get_item(a, k, gridDim.x);
         for (int j = 0; j < it.L; ++j) {
           int kb = block_of(a, it, j);
           if (kb < 0 || kb > it.I) kb = it.I;
@@ -320,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cnt[2] = {0, 0};
       bool ok = true;
       for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
-        const Item it = get_item(a, k);
+        const Item it = get_item(a, k, gridDim.x);
         if (!mbar_wait(q_full, item_idx & 1, a.err, abort_flag, tmo)) {
           ok = false;
           break;
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ns = 0, item_idx = 0;
     bool ok = true;
     for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
-      const Item it = get_item(a, k);
+      const Item it = get_item(a, k, gridDim.x);
       float m_run = -FLT_MAX, l_run = 0.f;
       for (int jj = t; jj < it.L; jj += 2) {
         if (!warp_wait(&s_full[t], ns & 1, a.err, abort_flag, tmo)) {
@@ -512,23 +524,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Counting sort of the selection's rows by descending length (longest first): the
-// attention kernel's CTAs take rows round-robin from this order, so every SM gets a
-// similar share of the work.  Rows of equal length keep no particular order.
-__global__ void order_hist_kernel(const int64_t* __restrict__ row_ptr, int rows, int* hist) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row < rows) atomicAdd(&hist[row_ptr[row + 1] - row_ptr[row]], 1);
+// Counting sort of the selection's rows by (KV head, descending length): the attention
+// kernel walks this order in serpentine waves (see get_item).  Rows with the same key keep
+// no particular order.
+__device__ __forceinline__ int order_key(const int64_t* row_ptr, int row, int nb, int hq, int hkv,
+                                         int group) {
+  const int h = row / nb;
+  const int hk = (h / hq) * hkv + (h % hq) / group;
+  const int len = static_cast<int>(row_ptr[row + 1] - row_ptr[row]);
+  return hk * (nb + 1) + (nb - len);
 }
 
-__global__ void __launch_bounds__(1024) order_scan_kernel(int* hist, int nb) {
-  // cursor[len] = number of rows longer than len, for len in [0, nb]
+__global__ void order_hist_kernel(const int64_t* __restrict__ row_ptr, int rows, int nb, int hq,
+                                  int hkv, int group, int* hist) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row < rows) atomicAdd(&hist[order_key(row_ptr, row, nb, hq, hkv, group)], 1);
+}
+
+// In-place exclusive scan of nbins counts (one CTA).
+__global__ void __launch_bounds__(1024) order_scan_kernel(int* hist, int nbins) {
   __shared__ int part[1024];
-  const int nbins = nb + 1;
   const int per = (nbins + 1023) / 1024;
-  // bins in descending length: position p holds length nb - p
   const int p0 = threadIdx.x * per, p1 = min(nbins, p0 + per);
   int s = 0;
-  for (int p = p0; p < p1; ++p) s += hist[nb - p];
+  for (int p = p0; p < p1; ++p) s += hist[p];
   part[threadIdx.x] = s;
   __syncthreads();
   for (int off = 1; off < 1024; off <<= 1) {
@@ -539,16 +558,16 @@ __global__ void __launch_bounds__(1024) order_scan_kernel(int* hist, int nb) {
   }
   int run = part[threadIdx.x] - s;
   for (int p = p0; p < p1; ++p) {
-    const int c = hist[nb - p];
-    hist[nb - p] = run;
+    const int c = hist[p];
+    hist[p] = run;
     run += c;
   }
 }
 
-__global__ void order_scatter_kernel(const int64_t* __restrict__ row_ptr, int rows, int* cursor,
-                                     int32_t* order) {
+__global__ void order_scatter_kernel(const int64_t* __restrict__ row_ptr, int rows, int nb, int hq,
+                                     int hkv, int group, int* cursor, int32_t* order) {
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row < rows) order[atomicAdd(&cursor[row_ptr[row + 1] - row_ptr[row]], 1)] = row;
+  if (row < rows) order[atomicAdd(&cursor[order_key(row_ptr, row, nb, hq, hkv, group)], 1)] = row;
 }
 
 }  // namespace
@@ -571,12 +590,14 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.dense = dense ? 1 : 0;
   if (!dense) {
     const int rows = s.H * s.nb;
-    cudaError_t e = cudaMemsetAsync(ctx->ws.len_hist, 0, sizeof(int) * (s.nb + 2), st);
+    const int nbins = s.Hkv * (s.nb + 1);
+    cudaError_t e = cudaMemsetAsync(ctx->ws.len_hist, 0, sizeof(int) * nbins, st);
     if (e != cudaSuccess) return e;
-    order_hist_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows, ctx->ws.len_hist);
-    order_scan_kernel<<<1, 1024, 0, st>>>(ctx->ws.len_hist, s.nb);
-    order_scatter_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows,
-                                                              ctx->ws.len_hist, ctx->ws.order);
+    order_hist_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows, s.nb, s.hq, s.hkv,
+                                                          s.group, ctx->ws.len_hist);
+    order_scan_kernel<<<1, 1024, 0, st>>>(ctx->ws.len_hist, nbins);
+    order_scatter_kernel<<<(rows + 255) / 256, 256, 0, st>>>(
+        ctx->ws.row_ptr, rows, s.nb, s.hq, s.hkv, s.group, ctx->ws.len_hist, ctx->ws.order);
   }
   a.O = static_cast<uint16_t*>(O);
   a.err = ctx->ws.err;

@@ -59,7 +59,7 @@ struct Workspace {
   int64_t col_cap = 0;
   // attention work order: rows sorted by descending length (counting sort)
   int32_t* order = nullptr;     // [H*nb]
-  int32_t* len_hist = nullptr;  // [nb+2] histogram, then cursors
+  int32_t* len_hist = nullptr;  // [Hkv*(nb+1)] histogram of (KV head, length), then cursors
   uint32_t* err = nullptr;      // device error word
 };
 
