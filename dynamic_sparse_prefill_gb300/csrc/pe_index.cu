@@ -190,10 +190,12 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
   if (route[h]) return;
   const PeState st = pe[h];
   if (st.select_all) return;
+  // Per-CTA histogram with native fp32 shared-memory atomics; the CTA's partial masses
+  // (each at most a few percent of the total) are combined in fp64 in global memory.
   __shared__ unsigned int scnt[256];
-  __shared__ double smass[256];
+  __shared__ float smass[256];
   scnt[threadIdx.x] = 0;
-  smass[threadIdx.x] = 0.0;
+  smass[threadIdx.x] = 0.f;
   __syncthreads();
   // Each thread keeps a run (bin, count, fp32 mass) and flushes it to the shared
   // histogram only when the bin changes: the early passes see long runs of one bin.
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
     if (bin != cur) {
       if (cnt) {
         atomicAdd(&scnt[cur], cnt);
-        atomicAdd(&smass[cur], static_cast<double>(mass));
+        atomicAdd(&smass[cur], mass);
       }
       cur = bin;
       cnt = 0;
@@ -241,12 +243,12 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
   }
   if (cnt) {
     atomicAdd(&scnt[cur], cnt);
-    atomicAdd(&smass[cur], static_cast<double>(mass));
+    atomicAdd(&smass[cur], mass);
   }
   __syncthreads();
   if (scnt[threadIdx.x]) {
     atomicAdd(&hist_cnt[h * 256 + threadIdx.x], static_cast<unsigned long long>(scnt[threadIdx.x]));
-    atomicAdd(&hist_mass[h * 256 + threadIdx.x], smass[threadIdx.x]);
+    atomicAdd(&hist_mass[h * 256 + threadIdx.x], static_cast<double>(smass[threadIdx.x]));
   }
 }
 

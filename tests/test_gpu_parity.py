@@ -310,3 +310,26 @@ def test_jsd_routing_diagnostic(dsp, name):
         ctx.selection_set(dims, rp, np.tile(np.arange(nb, dtype=np.int32), w.hq))
         ctx.jsd(dims, q, k, tau, d_js, route)
     ctx.close()
+
+
+def test_batch_two_matches_flattened_heads(dsp):
+    """batch = 2 with (hq, hkv) = (4, 2) addresses the same heads and KV heads as batch = 1
+    with (8, 4): routes, selections and outputs must be bit-identical; the flattened case
+    also holds oracle parity."""
+    w = Workload("batch_flat", n=4096, hq=8, hkv=4, seed=77, pe_heads=(1, 6),
+                 needles=("uniform", 2, 6))
+    g = generate(w)
+    run_parity(dsp, w, g)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    outs, sels = [], []
+    for dims in (dsp.make_dims(1, w.n, 8, 4), dsp.make_dims(2, w.n, 4, 2)):
+        ctx = dsp.Context(dims)
+        o = torch.empty_like(q)
+        ctx.prefill(dims, q, k, v, _cfg(dsp, w), o)
+        assert ctx.sync_status() == 0
+        sels.append(ctx.selection_get(dims))
+        outs.append(o.clone())
+        ctx.close()
+    for key in ("route_vs", "c_struct", "sel_v", "sel_s", "row_ptr", "col"):
+        assert np.array_equal(sels[0][key], sels[1][key]), key
+    assert torch.equal(outs[0], outs[1])
