@@ -380,8 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(tmem + t * 128, sdesc_sw128(q_base + off, 16, 1024),
                       sdesc_sw128(k_base + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
           }
+          // (the K slot is released by the softmax warpgroup when it sees s_full: one
+          // tcgen05.commit less per block)
           umma_commit(&s_full[t]);
-          umma_commit(&k_empty[s]);
           ++gk;
           if (j == it.L - 1) umma_commit(q_empty);
           if (j >= 1 && !do_pv(j - 1)) ok = false;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + t * 128;
     const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
-    int ns = 0, item_idx = 0;
+    int ns = 0, item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
     bool ok = true;
     for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
       const Item it = get_item(a, k, gridDim.x);
@@ -416,6 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ns;
         tc_fence_after();
+        // S_j is complete, so K_j's ring slot is free again.
+        if ((warp & 3) == 0 && lane == 0) mbar_arrive(&k_empty[(gbase + jj) % kKStages]);
         const bool diag = block_of(a, it, jj) == it.I;
         const bool first = (jj == t);
         // The whole S row in one TMEM round trip.
@@ -466,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           item_idx == 0 && jj + 2 >= it.L;
         if (!drop) mbar_arrive(&p_full[t]);
       }
+      gbase += it.L;
       if (!ok) break;
       // ---- epilogue: merge the two tiles' partial softmaxes, write this tile's half
       const int par = item_idx & 1;

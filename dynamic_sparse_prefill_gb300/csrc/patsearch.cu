@@ -24,7 +24,7 @@ namespace crisp {
 
 namespace {
 
-constexpr int kProxyThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kProxyThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2-9: epilogue
 constexpr int kProxyStages = 4;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr size_t kProxySmem = 1024 + kTileBytes * (1 + kProxyStages) + 256;
@@ -163,71 +163,91 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       drain_wait(drain, 0, a.err, tmo);
     }
   } else {
-    // Epilogue: thread <-> proxy row r (TMEM lane), 4 warps cover the 4 lane quarters.
+    // Epilogue: two warpgroups, warpgroup e takes the tiles i with (i & 1) == e, i.e. the
+    // S buffer e; thread <-> proxy row r (TMEM lane).  Each warpgroup exponentiates
+    // against its running row maximum m_run and falls back to the tile's exact maximum
+    // only when the sums show the tile exceeds m_run by a lot (the combine kernels accept
+    // any per-tile reference maximum).
+    const int e = (warp - 2) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const uint32_t row_taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    for (int i = 0; i < ntiles; ++i) {
-      const int sb = i & 1;
-      if (!warp_wait(&s_full[sb], (i >> 1) & 1, a.err, abort_flag, tmo)) break;
+    const uint32_t row_taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + e * 128;
+    float m_run = -FLT_MAX;
+    bool have_m = false;
+    for (int i = e; i < ntiles; i += 2) {
+      if (!warp_wait(&s_full[e], (i >> 1) & 1, a.err, abort_flag, tmo)) break;
       tc_fence_after();
-      uint32_t v[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(row_taddr + sb * 128 + c * 32, v[c]);
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
-
       const int t = t_begin + i;
       const bool last = (t == a.nb - 1);
       const int j0 = t * kBlk;
-      // Row maximum over the tile's visible keys (the last tile is causal: c <= r),
-      // eight independent chains.
-      float mx[8];
+      // u: keys with c <= r (slash block N_b-1-t); w: keys with c > r (slash block
+      // N_b-2-t); the last tile is causal (c <= r only).
+      auto sums = [&](float m, float& u, float& w) {
+        float uu[4] = {0.f, 0.f, 0.f, 0.f}, ww[4] = {0.f, 0.f, 0.f, 0.f};
+        const float neg = -m;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = -FLT_MAX;
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(row_taddr + c4 * 32, v);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = c4 * 32 + c;
-          if (!last || col <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c4][c]));
+          for (int c = 0; c < 32; ++c) {
+            const int col = c4 * 32 + c;
+            const float x = fast_exp2(fmaf(__uint_as_float(v[c]), a.scale_log2, neg));
+            if (col <= r)
+              uu[c & 3] += x;
+            else if (!last)
+              ww[c & 3] += x;
+          }
         }
-      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m2 = mraw * a.scale_log2;
-      const float neg = -m2;
-      // u: keys with c <= r (slash block N_b-1-t), w: keys with c > r (slash block N_b-2-t)
-      float uu[4] = {0.f, 0.f, 0.f, 0.f}, ww[4] = {0.f, 0.f, 0.f, 0.f};
+        u = (uu[0] + uu[1]) + (uu[2] + uu[3]);
+        w = (ww[0] + ww[1]) + (ww[2] + ww[3]);
+      };
+      float u = 0.f, w = 0.f;
+      bool slow = !have_m;
+      if (!slow) {
+        sums(m_run, u, w);
+        slow = __any_sync(0xffffffffu, !(u + w <= 32768.f));
+      }
+      if (slow) {
+        float mx[8];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
+        for (int k = 0; k < 8; ++k) mx[k] = -FLT_MAX;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = c4 * 32 + c;
-          const float e = fast_exp2(fmaf(__uint_as_float(v[c4][c]), a.scale_log2, neg));
-          if (col <= r)
-            uu[c & 3] += e;
-          else if (!last)
-            ww[c & 3] += e;
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(row_taddr + c4 * 32, v);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (!last || c4 * 32 + c <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
         }
-      const float u = (uu[0] + uu[1]) + (uu[2] + uu[3]);
-      const float w = (ww[0] + ww[1]) + (ww[2] + ww[3]);
+        const float ms = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
+        if (!have_m || ms > m_run) m_run = ms;
+        have_m = true;
+        sums(m_run, u, w);
+      }
       // Anchor mass: the first w_sink keys (tile 0) and the last w_local keys (last tile).
       float an = 0.f;
       if (t == 0 || last) {
+        const float neg = -m_run;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(row_taddr + c4 * 32, v);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int col = c4 * 32 + c;
             const int j = j0 + col;
             const bool valid = !last || col <= r;
             const bool anchor = (t == 0 && j < a.w_sink) || (last && j >= a.n - a.w_local);
-            if (valid && anchor) an += fast_exp2(fmaf(__uint_as_float(v[c4][c]), a.scale_log2, neg));
+            if (valid && anchor) an += fast_exp2(fmaf(__uint_as_float(v[c]), a.scale_log2, neg));
           }
+        }
       }
-      const float mx_out = m2;
+      tc_fence_before();
+      mbar_arrive(&s_free[e]);
       const size_t idx = (static_cast<size_t>(h) * a.nb + t) * kBlk + r;
-      a.st_m[idx] = mx_out;
+      a.st_m[idx] = m_run;
       a.st_u[idx] = u;
       a.st_w[idx] = w;
       if (t == 0) {
