@@ -35,8 +35,9 @@ UNIT = "ms/layer"
 B = 128
 D = 128
 # Kernel launches of one crisp_prefill: PatSearch 4, PEIndex 16, CSR 4, work order 3,
-# attention 1.
-LAUNCHES_PER_PREFILL = 28
+# attention 2 (the fast pass and the rescue pass, which returns at once when no row was
+# listed).
+LAUNCHES_PER_PREFILL = 29
 
 
 def algorithmic_flops(nnz: int, rows: int) -> float:

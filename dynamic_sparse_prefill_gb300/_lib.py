@@ -26,7 +26,8 @@ DEBUG_DROP_ARRIVE = 0x1
 EXPORTED = ["crisp_cfg_default", "crisp_create", "crisp_destroy", "crisp_select", "crisp_attend",
             "crisp_prefill", "crisp_dense", "crisp_selection_get", "crisp_selection_set",
             "crisp_selection_stats", "crisp_sync_status", "crisp_set_debug",
-            "crisp_status_string", "crisp_last_error", "crisp_route_static", "crisp_jsd"]
+            "crisp_status_string", "crisp_last_error", "crisp_route_static", "crisp_jsd",
+            "crisp_attend_info"]
 
 
 class Dims(ctypes.Structure):
@@ -79,6 +80,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "crisp_selection_get": (ctypes.c_int, [P, DP, P, ctypes.POINTER(SelectionHost)]),
         "crisp_selection_set": (ctypes.c_int, [P, DP, P, P, P, ctypes.c_int64]),
         "crisp_selection_stats": (ctypes.c_int, [P, DP, P, ctypes.POINTER(Stats)]),
+        "crisp_attend_info": (ctypes.c_int, [P, P, ctypes.POINTER(ctypes.c_int64)]),
         "crisp_sync_status": (ctypes.c_int, [P, P]),
         "crisp_set_debug": (ctypes.c_int, [P, ctypes.c_uint32, ctypes.c_uint64]),
         "crisp_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -173,6 +175,13 @@ class Context:
         self._check(self._lib.crisp_jsd(self._h, ctypes.byref(dims), _ptr(q), _ptr(k),
                                         ctypes.c_float(tau_jsd), _ptr(d_js), _ptr(route_vs),
                                         _stream(stream)), "crisp_jsd")
+
+    def attend_info(self, stream=None) -> int:
+        """Query-block rows the last attend/dense recomputed in the rescue pass."""
+        rows = ctypes.c_int64(0)
+        self._check(self._lib.crisp_attend_info(self._h, _stream(stream), ctypes.byref(rows)),
+                    "crisp_attend_info")
+        return rows.value
 
     def sync_status(self, stream=None) -> int:
         return self._lib.crisp_sync_status(self._h, _stream(stream))

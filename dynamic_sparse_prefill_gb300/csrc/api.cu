@@ -220,6 +220,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.col), sizeof(int32_t) * w.col_cap},
       {reinterpret_cast<void**>(&w.order), sizeof(int32_t) * H * nb},
       {reinterpret_cast<void**>(&w.len_hist), sizeof(int32_t) * (Hkv * (nb + 1) + 2)},
+      {reinterpret_cast<void**>(&w.redo), sizeof(int32_t) * H * nb},
+      {reinterpret_cast<void**>(&w.redo_count), sizeof(int)},
       {reinterpret_cast<void**>(&w.err), sizeof(uint32_t)},
   };
   size_t total = 0;
@@ -235,7 +237,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
     *pc.p = static_cast<char*>(base) + off;
     off += (pc.bytes + 255) & ~static_cast<size_t>(255);
   }
-  if (cudaMemset(w.err, 0, sizeof(uint32_t)) != cudaSuccess) {
+  if (cudaMemset(w.err, 0, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(w.redo_count, 0, sizeof(int)) != cudaSuccess) {
     cudaFree(base);
     delete ctx;
     return CRISP_ERR_CUDA;
@@ -428,6 +431,16 @@ crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* 
       out->pe_rescued += counts[4 * h + 1];
     }
   }
+  return CRISP_OK;
+}
+
+crisp_status crisp_attend_info(crisp_ctx ctx, void* stream, int64_t* rows) {
+  if (!ctx || !rows) return CRISP_ERR_INVALID_ARG;
+  crisp_status st = launched(ctx, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "sync");
+  if (st != CRISP_OK) return st;
+  int count = 0;
+  if ((st = copy_out(ctx, &count, ctx->ws.redo_count, sizeof(int))) != CRISP_OK) return st;
+  *rows = count;
   return CRISP_OK;
 }
 

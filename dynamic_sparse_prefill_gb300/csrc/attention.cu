@@ -7,21 +7,28 @@
 // "Method step details" step 4 applies it to the selected index set.  With every key
 // block K <= I selected this is dense causal attention, the speedup denominator.
 //
-// Persistent kernel: one CTA per SM walks work items (query head h, query block I) in
-// serpentine waves over an order that keeps each KV head's rows together, longest first
-// (see get_item).  Ten warps:
+// Two persistent kernels, one CTA per SM, walking work items (query head h, query block
+// I) in serpentine waves over an order that keeps each KV head's rows together, longest
+// first (see get_item).  Both use the same warp roles:
 //   warps 0-3  softmax of "tile 0": the even-numbered key blocks of the item's list;
 //   warps 4-7  softmax of "tile 1": the odd-numbered key blocks;
 //   warp 8     TMA producer of the item's Q tile and K_j (3-slot ring);
-//   warp 9     MMA issuer (one thread, tcgen05): S = Q K_j^T into TMEM, then
-//              O_t += P V_j with P read from TMEM;
+//   warp 9     MMA issuer (one thread, tcgen05): S = Q K_j^T into TMEM, then O += P V_j
+//              with P read from TMEM;
 //   warp 10    TMA producer of V_j (2-slot ring), so K prefetch never waits on a V slot.
 // The softmax warpgroups take registers from the loader warpgroup (setmaxnreg).
-// The two tiles share the item's Q tile but keep their own S buffer, running max/sum
-// and O accumulator in TMEM, so the tensor core works on one tile while the other's
-// softmax runs; the epilogue merges the two partial softmaxes exactly.  P overwrites
-// its S buffer as packed bf16.  The running max is only raised when a block exceeds it
-// by more than 2^8, so the O rescale (TMEM load, scale, store) is rare.
+//
+// attention_kernel (every item): each tile has its own S and P buffers in TMEM and the
+// two tiles accumulate into one O, exponentiating against one reference per row (the
+// larger of the exact maxima of the tiles' first blocks).  A tile's next S is computed
+// while its softmax still works on the previous one, so the tensor core never waits for
+// a P to be written before it can start the next S.  Rows whose P could overflow against
+// the reference are listed for the rescue pass.
+//
+// attention_rescue_kernel (the listed rows only; normally none): each tile keeps its own
+// running max, sum and O accumulator, P overwrites its S buffer, and the epilogue merges
+// the two partial softmaxes exactly.  The running max is raised (with a TMEM rescale of
+// O) when a block exceeds it by more than 2^8, so any finite input is handled.
 // All waits are bounded (see ptx.cuh); nothing traps.
 #include <cuda_bf16.h>
 
@@ -37,12 +44,17 @@ namespace {
 // WG2 (warps 8-11): warp 8 Q/K producer, warp 9 MMA issuer, warp 10 V producer.
 constexpr int kThreads = 384;
 // Register split: launched at kLaunchRegs per thread (the host checks the compiled
-// count), the softmax warpgroups grow to kSoftmaxRegs and WG2 shrinks to kLoaderRegs:
-// 128 * (2 * 232 + 40) = 64512 = 384 * 168.
+// count), the softmax warpgroups grow and WG2 shrinks; the sum must fit the launch
+// allocation.  The fast pass: 128 * (2 * 224 + 56) = 64512 = 384 * 168.  The rescue pass
+// (heavier softmax, with O rescaling): 128 * (2 * 232 + 40) = 64512.
 constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 232;
-constexpr uint32_t kLoaderRegs = 40;
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kLoaderRegs = 56;
+constexpr uint32_t kRescueSoftmaxRegs = 232;
+constexpr uint32_t kRescueLoaderRegs = 40;
 static_assert(128 * (2 * kSoftmaxRegs + kLoaderRegs) <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+static_assert(128 * (2 * kRescueSoftmaxRegs + kRescueLoaderRegs) <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
@@ -146,6 +158,13 @@ struct AttnArgs {
   uint32_t* err;
   uint64_t timeout_ns;
   uint32_t debug;
+  // Rescue pass: items are the rows listed in list[0 .. *list_count) (set by the fast pass).
+  const int32_t* list;
+  const int* list_count;
+  // Fast pass: rows whose probabilities could overflow against the row's reference
+  // maximum are appended here for the rescue pass.
+  int32_t* redo;
+  int* redo_count;
 };
 
 struct Item {
@@ -159,13 +178,17 @@ struct Item {
 // advance together over the same key blocks -- the order keeps one KV head's rows
 // together, so those blocks are fetched from DRAM once per wave and served from L2.
 // Dense order: KV head major, then query block descending, then the group's q-heads.
-__device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G) {
+__device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G, int num_items) {
   const int m = k / G, pos = k % G;
   const int base = m * G;
-  const int wsize = min(G, a.num_items - base);
+  const int wsize = min(G, num_items - base);
   const int ke = (m & 1) ? base + wsize - 1 - pos : k;
   Item it;
-  if (a.dense) {
+  if (a.list != nullptr) {
+    const int row = a.list[ke];
+    it.h = row / a.nb;
+    it.I = row % a.nb;
+  } else if (a.dense) {
     const int per_kv = a.group * a.nb;
     const int hk_all = ke / per_kv, r = ke % per_kv;
     it.I = a.nb - 1 - r / a.group;
@@ -191,10 +214,94 @@ __device__ __forceinline__ int block_of(const AttnArgs& a, const Item& it, int j
   return a.dense ? j : a.col[it.beg + j];
 }
 
+// TMA producer of the items' Q tiles and key blocks K_j (one thread): Q is reloaded once
+// the MMA warp has committed the item's last S (q_empty); K_j goes into a kKStages-slot
+// ring whose slots the consumer releases on k_empty.  Column indices outside [0, I] are
+// replaced by I and flagged (kErrRange).
+__device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, const CUtensorMap* tmQ,
+                                           const CUtensorMap* tmK, uint8_t* sQ, uint8_t* sK,
+                                           uint64_t* q_full, uint64_t* q_empty, uint64_t* k_full,
+                                           uint64_t* k_empty, volatile int* abort_flag,
+                                           uint64_t tmo) {
+  tma_prefetch_desc(tmQ);
+  tma_prefetch_desc(tmK);
+  int gk = 0, item_idx = 0, q_loads = 0;
+  bool ok = true;
+  for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
+    const Item it = get_item(a, k, gridDim.x, num_items);
+    if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) {
+      ok = false;
+      break;
+    }
+    const int qrow = it.h * a.n + it.I * kBlk;
+    mbar_arrive_expect_tx(q_full, kTileBytes);
+    tma_load_2d(sQ, tmQ, q_full, 0, qrow);
+    tma_load_2d(sQ + kTileBytes / 2, tmQ, q_full, 64, qrow);
+    ++q_loads;
+    for (int j = 0; j < it.L; ++j) {
+      int kb = block_of(a, it, j);
+      if (kb < 0 || kb > it.I) {
+        atomicOr(a.err, kErrRange);
+        kb = it.I;
+      }
+      const int s = gk % kKStages;
+      if (gk >= kKStages &&
+          !mbar_wait(&k_empty[s], ((gk / kKStages) + 1) & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = sK + s * kTileBytes;
+      const int row = it.hk * a.n + kb * kBlk;
+      mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+      tma_load_2d(dst, tmK, &k_full[s], 0, row);
+      tma_load_2d(dst + kTileBytes / 2, tmK, &k_full[s], 64, row);
+      ++gk;
+    }
+  }
+  // Let every copy still in flight land before the CTA can exit.
+  if (q_loads > 0) drain_wait(q_full, (q_loads - 1) & 1, a.err, tmo);
+  for (int g = max(0, gk - kKStages); g < gk; ++g)
+    drain_wait(&k_full[g % kKStages], (g / kKStages) & 1, a.err, tmo);
+}
+
+// TMA producer of the value blocks V_j (one thread) into a kVStages-slot ring, released by
+// the commit after the P.V MMAs that read the slot (v_empty).
+__device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, const CUtensorMap* tmV,
+                                          uint8_t* sV, uint64_t* v_full, uint64_t* v_empty,
+                                          volatile int* abort_flag, uint64_t tmo) {
+  tma_prefetch_desc(tmV);
+  int gv = 0;
+  bool ok = true;
+  for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x) {
+    const Item it = get_item(a, k, gridDim.x, num_items);
+    for (int j = 0; j < it.L; ++j) {
+      int kb = block_of(a, it, j);
+      if (kb < 0 || kb > it.I) kb = it.I;
+      const int s = gv % kVStages;
+      if (gv >= kVStages &&
+          !mbar_wait(&v_empty[s], ((gv / kVStages) + 1) & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = sV + s * kTileBytes;
+      const int row = it.hk * a.n + kb * kBlk;
+      mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+      tma_load_2d(dst, tmV, &v_full[s], 0, row);
+      tma_load_2d(dst + kTileBytes / 2, tmV, &v_full[s], 64, row);
+      ++gv;
+    }
+  }
+  for (int g = max(0, gv - kVStages); g < gv; ++g)
+    drain_wait(&v_full[g % kVStages], (g / kVStages) & 1, a.err, tmo);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    attention_kernel(const __grid_constant__ CUtensorMap tmQ,
+    attention_rescue_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  // The rescue pass is launched on a full grid before the number of listed rows is known.
+  const int num_items = a.list_count != nullptr ? *a.list_count : a.num_items;
+  if (static_cast<int>(blockIdx.x) >= num_items) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -252,78 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp >= 8) {
-    regs_decrease<kLoaderRegs>();
+    regs_decrease<kRescueLoaderRegs>();
   if (warp == 8) {
-    // ------------------------------------------------------------------ TMA producer: Q, K
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      int gk = 0, item_idx = 0, q_loads = 0;
-      bool ok = true;
-      for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
-        const Item it = get_item(a, k, gridDim.x);
-        if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) {
-          ok = false;
-          break;
-        }
-        const int qrow = it.h * a.n + it.I * kBlk;
-        mbar_arrive_expect_tx(q_full, kTileBytes);
-        tma_load_2d(sQ, &tmQ, q_full, 0, qrow);
-        tma_load_2d(sQ + kTileBytes / 2, &tmQ, q_full, 64, qrow);
-        ++q_loads;
-        for (int j = 0; j < it.L; ++j) {
-          int kb = block_of(a, it, j);
-          if (kb < 0 || kb > it.I) {
-            atomicOr(a.err, kErrRange);
-            kb = it.I;
-          }
-          const int s = gk % kKStages;
-          if (gk >= kKStages &&
-              !mbar_wait(&k_empty[s], ((gk / kKStages) + 1) & 1, a.err, abort_flag, tmo)) {
-            ok = false;
-            break;
-          }
-          uint8_t* dst = sK + s * kTileBytes;
-          const int row = it.hk * a.n + kb * kBlk;
-          mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-          tma_load_2d(dst, &tmK, &k_full[s], 0, row);
-          tma_load_2d(dst + kTileBytes / 2, &tmK, &k_full[s], 64, row);
-          ++gk;
-        }
-      }
-      // Let every copy still in flight land before the CTA can exit.
-      if (q_loads > 0) drain_wait(q_full, (q_loads - 1) & 1, a.err, tmo);
-      for (int g = max(0, gk - kKStages); g < gk; ++g)
-        drain_wait(&k_full[g % kKStages], (g / kKStages) & 1, a.err, tmo);
-    }
+    if (lane == 0)
+      produce_qk(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full, k_empty, abort_flag, tmo);
   } else if (warp == 10) {
-    // ------------------------------------------------------------------ TMA producer: V
-    if (lane == 0) {
-      tma_prefetch_desc(&tmV);
-      int gv = 0;
-      bool ok = true;
-      for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x) {
-        const Item it = get_item(a, k, gridDim.x);
-        for (int j = 0; j < it.L; ++j) {
-          int kb = block_of(a, it, j);
-          if (kb < 0 || kb > it.I) kb = it.I;
-          const int s = gv % kVStages;
-          if (gv >= kVStages &&
-              !mbar_wait(&v_empty[s], ((gv / kVStages) + 1) & 1, a.err, abort_flag, tmo)) {
-            ok = false;
-            break;
-          }
-          uint8_t* dst = sV + s * kTileBytes;
-          const int row = it.hk * a.n + kb * kBlk;
-          mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-          tma_load_2d(dst, &tmV, &v_full[s], 0, row);
-          tma_load_2d(dst + kTileBytes / 2, &tmV, &v_full[s], 64, row);
-          ++gv;
-        }
-      }
-      for (int g = max(0, gv - kVStages); g < gv; ++g)
-        drain_wait(&v_full[g % kVStages], (g / kVStages) & 1, a.err, tmo);
-    }
+    if (lane == 0) produce_v(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -331,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gk = 0, gv = 0, item_idx = 0;
       int cnt[2] = {0, 0};
       bool ok = true;
-      for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
-        const Item it = get_item(a, k, gridDim.x);
+      for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
+        const Item it = get_item(a, k, gridDim.x, num_items);
         if (!mbar_wait(q_full, item_idx & 1, a.err, abort_flag, tmo)) {
           ok = false;
           break;
@@ -397,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    regs_increase<kSoftmaxRegs>();
+    regs_increase<kRescueSoftmaxRegs>();
     // ------------------------------------------------------------------ softmax / epilogue
     const int t = warp >> 2;         // tile: 0 for warps 0-3, 1 for warps 4-7
     const int q = warp & 3;          // TMEM lane quarter this warp may access
@@ -407,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
     int ns = 0, item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
     bool ok = true;
-    for (int k = blockIdx.x; k < a.num_items && ok; k += gridDim.x, ++item_idx) {
-      const Item it = get_item(a, k, gridDim.x);
+    for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
+      const Item it = get_item(a, k, gridDim.x, num_items);
       float m_run = -FLT_MAX, l_run = 0.f;
       for (int jj = t; jj < it.L; jj += 2) {
         if (!warp_wait(&s_full[t], ns & 1, a.err, abort_flag, tmo)) {
@@ -528,6 +569,305 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Fast pass.  TMEM: S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512).
+// Each tile's P has its own columns, so the MMA warp computes a tile's next S block as
+// soon as that tile's softmax has loaded the previous one, while the softmax is still
+// exponentiating it: the tensor core always holds queued work.  The price is one O
+// accumulator for both tiles, so both exponentiate against one reference per row: the
+// larger of the exact row maxima of the two tiles' first blocks, exchanged once per item.
+// The reference is never above the row's true maximum, so the largest P of the row is at
+// least 1 and nothing that matters underflows; a block whose P row sum passes 2^64 (a logit
+// more than 64 log2-units above the reference) marks its item for the rescue pass, which
+// recomputes the item with per-tile running maxima.
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
+constexpr float kOverflowSum = 18446744073709551616.0f;  // 2^64
+constexpr size_t kXBytes = 2 * 2 * kBlk * sizeof(float) + 16;  // row max, row sum per tile; flag
+constexpr size_t kSmemFast = 1024 + kTileBytes * (1 + kKStages + kVStages) + kXBytes + 512;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kTileBytes;
+  uint8_t* sV = sK + kKStages * kTileBytes;
+  float* sXM = reinterpret_cast<float*>(sV + kVStages * kTileBytes);  // [tile][row] first-block max
+  float* sXL = sXM + 2 * kBlk;                                         // [tile][row] row sum
+  volatile int* sRedo = reinterpret_cast<volatile int*>(sXL + 2 * kBlk);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sXM) + kXBytes);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;    // [3]
+  uint64_t* k_empty = bars + 5;   // [3]
+  uint64_t* v_full = bars + 8;    // [2]
+  uint64_t* v_empty = bars + 10;  // [2]
+  uint64_t* s_full = bars + 12;   // [2] S_t holds the tile's next block
+  uint64_t* s_free = bars + 14;   // [2] the tile's softmax has loaded S_t
+  uint64_t* p_full = bars + 16;   // [2] P_t written
+  uint64_t* p_free = bars + 18;   // [2] the P.V MMAs reading P_t have completed
+  uint64_t* o_done = bars + 20;
+  uint64_t* o_free = bars + 21;
+  uint64_t* x_ready = bars + 22;  // both tiles' first-block maxima are in sXM
+  uint64_t* l_ready = bars + 23;  // both tiles' row sums are in sXL
+  uint64_t* drain = bars + 24;    // [2] one per MMA-issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t tmo = a.timeout_ns;
+  const int num_items = a.num_items;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 4);   // one arrive per warp of the tile
+      mbar_init(&p_full[t], 4);
+      mbar_init(&p_free[t], 1);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 8);       // one arrive per softmax warp
+    mbar_init(x_ready, 8);
+    mbar_init(l_ready, 8);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
+    *sRedo = 0;
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp >= 8) {
+    regs_decrease<kLoaderRegs>();
+    if (warp == 8) {
+      if (lane == 0)
+        produce_qk(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full, k_empty, abort_flag,
+                   tmo);
+    } else if (warp == 10) {
+      if (lane == 0) produce_v(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
+    } else if (warp == 9) {
+      // ---------------------------------------------------------------- S issuer
+      // S_j = Q K_j^T into tile (j & 1)'s buffer, as soon as the tile's softmax has loaded
+      // the buffer's previous block.  tcgen05.mma issue waits for the tensor core, so S
+      // and P.V come from two threads: neither stream stalls the other while it waits.
+      if (lane == 0) {
+        const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+        int gk = 0, item_idx = 0;
+        int ns[2] = {0, 0};  // S blocks issued into S_t so far
+        bool ok = true;
+        for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
+          const Item it = get_item(a, k, gridDim.x, num_items);
+          if (!mbar_wait(q_full, item_idx & 1, a.err, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          for (int j = 0; j < it.L; ++j) {
+            const int t = j & 1;
+            const int s = gk % kKStages;
+            if ((ns[t] > 0 && !mbar_wait(&s_free[t], (ns[t] - 1) & 1, a.err, abort_flag, tmo)) ||
+                !mbar_wait(&k_full[s], (gk / kKStages) & 1, a.err, abort_flag, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // Descriptors advance by byte offset >> 4 in the start-address field.
+            const uint64_t dK = dK0 + static_cast<uint64_t>(s * (kTileBytes >> 4));
+            const uint32_t d = tmem + t * 128;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = ((kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32) >> 4;
+              umma_bf16(d, dQ + off, dK + off, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&s_full[t]);
+            if (j == it.L - 1) umma_commit(q_empty);
+            ++ns[t];
+            ++gk;
+          }
+        }
+        umma_commit(&drain[0]);
+        drain_wait(&drain[0], 0, a.err, tmo);
+      }
+    } else {
+      // ---------------------------------------------------------------- P.V issuer (warp 11)
+      // O += P_j V_j once P_j is written; the item's first group overwrites O, after the
+      // previous item's epilogue has read it (o_free).
+      if (lane == 0) {
+        const uint64_t dV0 = sdesc_sw128(smem_u32(sV), kTileBytes / 2, 1024);
+        int gv = 0, item_idx = 0;
+        int np[2] = {0, 0};  // P.V groups issued from P_t so far
+        bool ok = true;
+        for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
+          const Item it = get_item(a, k, gridDim.x, num_items);
+          for (int j = 0; j < it.L; ++j) {
+            const int t = j & 1;
+            const int s = gv % kVStages;
+            if (!mbar_wait(&p_full[t], np[t] & 1, a.err, abort_flag, tmo) ||
+                (j == 0 && item_idx > 0 &&
+                 !mbar_wait(o_free, (item_idx - 1) & 1, a.err, abort_flag, tmo)) ||
+                !mbar_wait(&v_full[s], (gv / kVStages) & 1, a.err, abort_flag, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dV = dV0 + static_cast<uint64_t>(s * (kTileBytes >> 4));
+            const uint32_t p = tmem + kColP + t * 64;
+            // B = V rows 16kk.. (keys): MN-major, 64-column regions 16 KB apart (LBO),
+            // 8-row groups 1024 B apart (SBO).  A = P_t from TMEM, 8 columns per K step.
+            umma_bf16_tmem_a(tmem + kColO, p, dV, kIdescPV, j > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 1; kk < 8; ++kk)
+              umma_bf16_tmem_a(tmem + kColO, p + kk * 8, dV + ((kk * 2048) >> 4), kIdescPV, 1u);
+            umma_commit(&v_empty[s]);
+            umma_commit(&p_free[t]);
+            ++np[t];
+            ++gv;
+          }
+          if (ok) umma_commit(o_done);
+        }
+        umma_commit(&drain[1]);
+        drain_wait(&drain[1], 0, a.err, tmo);
+      }
+    }
+  } else {
+    regs_increase<kSoftmaxRegs>();
+    // ------------------------------------------------------------------ softmax / epilogue
+    const int t = warp >> 2;         // tile: 0 for warps 0-3, 1 for warps 4-7
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;     // query row within the block
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + t * 128;
+    const uint32_t p_addr = tmem + lane_off + kColP + t * 64;
+    int ns = 0, npw = 0, item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
+    bool ok = true;
+    uint32_t v[128];
+    // Waits for the tile's next S block, loads it, hands the S buffer back to the MMA warp
+    // and releases K_j's ring slot (S_j complete means K_j has been read).
+    auto load_s = [&](int jj) -> bool {
+      if (!warp_wait(&s_full[t], ns & 1, a.err, abort_flag, tmo)) return false;
+      ++ns;
+      tc_fence_after();
+      if (q == 0 && lane == 0) mbar_arrive(&k_empty[(gbase + jj) % kKStages]);
+      tmem_ld128(s_addr, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[t]);
+      return true;
+    };
+    for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
+      const Item it = get_item(a, k, gridDim.x, num_items);
+      // Row reference: the larger of the two tiles' first-block row maxima.
+      float mfirst = -FLT_MAX;
+      if (t < it.L) {
+        if (!load_s(t)) {
+          ok = false;
+          break;
+        }
+        mfirst = (block_of(a, it, t) == it.I ? row_max<true>(v, r) : row_max<false>(v, r)) *
+                 a.scale_log2;
+      }
+      sXM[t * kBlk + r] = mfirst;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x_ready);
+      if (!warp_wait(x_ready, item_idx & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      const float M = fmaxf(sXM[r], sXM[kBlk + r]);
+      float l = 0.f;
+      bool ovf = false;
+      for (int jj = t; jj < it.L; jj += 2) {
+        if (jj != t && !load_s(jj)) {
+          ok = false;
+          break;
+        }
+        const float rs = block_of(a, it, jj) == it.I ? exp_pack<true>(v, a.scale_log2, M, r)
+                                                     : exp_pack<false>(v, a.scale_log2, M, r);
+        ovf |= !(rs <= kOverflowSum);
+        l += rs;
+        if (npw > 0 && !warp_wait(&p_free[t], (npw - 1) & 1, a.err, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st64p(p_addr, v);
+        tmem_st_wait();
+        tc_fence_before();
+        const bool drop = (a.debug & CRISP_DEBUG_DROP_ARRIVE) && blockIdx.x == 0 &&
+                          item_idx == 0 && jj + 2 >= it.L;
+        __syncwarp();
+        if (!drop && lane == 0) mbar_arrive(&p_full[t]);
+        ++npw;
+      }
+      gbase += it.L;
+      if (!ok) break;
+      // ---- epilogue: O / (l_0 + l_1); this tile writes columns [64t, 64t + 64)
+      sXL[t * kBlk + r] = l;
+      if (ovf) *sRedo = 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(l_ready);
+      if (!warp_wait(l_ready, item_idx & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      const float inv = 1.f / (sXL[r] + sXL[kBlk + r]);
+      if (threadIdx.x == 0 && *sRedo) {
+        *sRedo = 0;
+        a.redo[atomicAdd(a.redo_count, 1)] = it.h * a.nb + it.I;
+      }
+      if (!warp_wait(o_done, item_idx & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint16_t* orow = a.O + (static_cast<size_t>(it.h) * a.n + static_cast<size_t>(it.I) * kBlk + r) * kD + t * 64;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + kColO + t * 64 + hh * 32, o);
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+          uint4 pkt;
+          pkt.x = pack_bf16(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
+          pkt.y = pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+          pkt.z = pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+          pkt.w = pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + hh * 32 + c) = pkt;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // Counting sort of the selection's rows by (KV head, descending length): the attention
 // kernel walks this order in serpentine waves (see get_item).  Rows with the same key keep
 // no particular order.
@@ -607,8 +947,22 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.err = ctx->ws.err;
   a.timeout_ns = (ctx->debug_flags & CRISP_DEBUG_DROP_ARRIVE) ? 50000000ull : ctx->timeout_ns;
   a.debug = ctx->debug_flags;
+  a.list = nullptr;
+  a.list_count = nullptr;
+  a.redo = ctx->ws.redo;
+  a.redo_count = ctx->ws.redo_count;
+  cudaError_t e = cudaMemsetAsync(ctx->ws.redo_count, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
   const int grid = a.num_items < ctx->num_sms ? a.num_items : ctx->num_sms;
-  attention_kernel<<<grid, kThreads, kSmem, st>>>(tmQ, tmK, tmV, a);
+  attention_kernel<<<grid, kThreads, kSmemFast, st>>>(tmQ, tmK, tmV, a);
+  // Rescue pass over the rows the fast pass listed (usually none: each CTA then reads the
+  // count and returns).
+  AttnArgs r = a;
+  r.list = ctx->ws.redo;
+  r.list_count = ctx->ws.redo_count;
+  r.redo = nullptr;
+  r.redo_count = nullptr;
+  attention_rescue_kernel<<<ctx->num_sms, kThreads, kSmem, st>>>(tmQ, tmK, tmV, r);
   return cudaGetLastError();
 }
 
@@ -619,7 +973,13 @@ cudaError_t init_attention_attributes() {
   cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel);
   if (e != cudaSuccess) return e;
   if (static_cast<uint32_t>(fa.numRegs) != kLaunchRegs) return cudaErrorInvalidKernelImage;
-  return cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncGetAttributes(&fa, attention_rescue_kernel);
+  if (e != cudaSuccess) return e;
+  if (static_cast<uint32_t>(fa.numRegs) != kLaunchRegs) return cudaErrorInvalidKernelImage;
+  e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemFast));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attention_rescue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmem));
 }
 

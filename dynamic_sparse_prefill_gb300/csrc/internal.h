@@ -60,6 +60,9 @@ struct Workspace {
   // attention work order: rows sorted by descending length (counting sort)
   int32_t* order = nullptr;     // [H*nb]
   int32_t* len_hist = nullptr;  // [Hkv*(nb+1)] histogram of (KV head, length), then cursors
+  // rows the fast attention pass hands to the rescue pass (see attention.cu)
+  int32_t* redo = nullptr;      // [H*nb]
+  int* redo_count = nullptr;
   uint32_t* err = nullptr;      // device error word
 };
 

@@ -179,6 +179,13 @@ crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* 
 crisp_status crisp_jsd(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
                        float tau_jsd, float* d_js, uint8_t* route_vs, void* stream);
 
+/* Synchronise `stream`, then write to *rows the number of query-block rows the last
+ * crisp_attend / crisp_dense on this context recomputed in its rescue pass.  The attention
+ * kernel exponentiates every row against one reference (the larger of two first-block row
+ * maxima); a row with a logit more than 64 log2-units above it is recomputed with running
+ * maxima ("Prerequisites": exact softmax attention either way).  Normally 0. */
+crisp_status crisp_attend_info(crisp_ctx ctx, void* stream, int64_t* rows);
+
 /* Synchronise `stream`, then report and clear the device error word: CRISP_OK,
  * CRISP_ERR_TIMEOUT or CRISP_ERR_DEVICE_ASSERT, or CRISP_ERR_CUDA if the stream itself
  * reports a CUDA error. */

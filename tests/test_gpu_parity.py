@@ -157,6 +157,7 @@ def test_dense_matches_oracle_and_sdpa(dsp):
     o = torch.empty_like(q)
     ctx.dense(dims, q, k, v, o)
     assert ctx.sync_status() == 0
+    assert ctx.attend_info() == 0   # no row of these inputs needs the rescue pass
     from oracle import crisp_oracle as O
     nb = w.n_blocks
     full = np.tril(np.ones((nb, nb), bool))
@@ -173,6 +174,60 @@ def test_dense_matches_oracle_and_sdpa(dsp):
     sd = torch.nn.functional.scaled_dot_product_attention(q[None], kk, vv, is_causal=True)[0]
     d = (sd.float() - o.float()).abs()
     assert float(d.max()) < 2e-2 and float(d.mean()) < 2e-3
+    ctx.close()
+
+
+def test_rescue_pass_recomputes_overflowing_rows(dsp):
+    """The attention kernel exponentiates a row against one reference, the larger of the
+    exact row maxima of its two first key blocks.  Three query rows of block 5 and one key
+    of block 3 share a component of 30 (logit ~115 log2-units above the reference), which
+    would overflow: the item must go to the rescue pass (running maxima) and still match
+    the oracle's exact softmax, through crisp_dense and through a hand-set sparse
+    selection; a selection without block 3 needs no rescue."""
+    from oracle import crisp_oracle as O
+    from workloads.planted import f32_to_bf16_bits
+    n, hq, hkv = 1024, 2, 1
+    nb = n // 128
+    g = random_qkv(n, hq, hkv, 128, seed=41, scale=4.0)
+    q, k, v = g["q"].copy(), g["k"].copy(), g["v"]
+    big = f32_to_bf16_bits(np.float32([30.0]))[0]
+    for r in (5 * 128 + 3, 5 * 128 + 64, 5 * 128 + 127):
+        q[0, r, :] = 0
+        q[0, r, 1] = big
+    k[0, 3 * 128 + 7, :] = 0
+    k[0, 3 * 128 + 7, 1] = big
+    dq, dk, dv = to_device(q), to_device(k), to_device(v)
+    dims = dsp.make_dims(1, n, hq, hkv)
+    ctx = dsp.Context(dims)
+    qf = [O.bf16_bits_to_f64(q[h]) for h in range(hq)]
+    kf, vf = O.bf16_bits_to_f64(k[0]), O.bf16_bits_to_f64(v[0])
+
+    o = torch.empty_like(dq)
+    ctx.dense(dims, dq, dk, dv, o)
+    assert ctx.sync_status() == 0
+    assert ctx.attend_info() == 1
+    got = o.float().cpu().numpy()
+    full = np.tril(np.ones((nb, nb), bool))
+    for h in range(hq):
+        ref = O.block_sparse_attention(qf[h], kf, vf, full, 128, list(range(nb)))
+        compare_outputs(got[h], ref, f"dense with rescue, head {h}")
+
+    for with_key, rescued in ((True, 1), (False, 0)):
+        masks = [np.eye(nb, dtype=bool) for _ in range(hq)]
+        masks[0][:, 0] = True
+        masks[0][5, 1] = True          # blocks 0 and 1 are the row's first blocks
+        if with_key:
+            masks[0][5, 3] = True      # third block: above the reference by ~110 log2-units
+        rp, col = csr_from_masks(masks, nb)
+        ctx.selection_set(dims, rp, col)
+        o2 = torch.empty_like(dq)
+        ctx.attend(dims, dq, dk, dv, o2)
+        assert ctx.sync_status() == 0
+        assert ctx.attend_info() == rescued
+        got = o2.float().cpu().numpy()
+        for h in range(hq):
+            ref = O.block_sparse_attention(qf[h], kf, vf, np.tril(masks[h]), 128, list(range(nb)))
+            compare_outputs(got[h], ref, f"sparse with_key={with_key}, head {h}")
     ctx.close()
 
 
@@ -242,6 +297,7 @@ def test_llama_n512k_sampled_and_dense(dsp):
     o = torch.empty_like(q)
     ctx.dense(dims, q, k, v, o)
     assert ctx.sync_status() == 0
+    assert ctx.attend_info() == 0   # no row of these inputs needs the rescue pass
     from oracle import crisp_oracle as O
     nb = w.n_blocks
     full = np.tril(np.ones((nb, nb), bool))
