@@ -218,6 +218,7 @@ __device__ __forceinline__ int block_of(const AttnArgs& a, const Item& it, int j
 // the MMA warp has committed the item's last S (q_empty); K_j goes into a kKStages-slot
 // ring whose slots the consumer releases on k_empty.  Column indices outside [0, I] are
 // replaced by I and flagged (kErrRange).
+template <int kKS>
 __device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, const CUtensorMap* tmQ,
                                            const CUtensorMap* tmK, uint8_t* sQ, uint8_t* sK,
                                            uint64_t* q_full, uint64_t* q_empty, uint64_t* k_full,
@@ -244,9 +245,9 @@ __device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, con
         atomicOr(a.err, kErrRange);
         kb = it.I;
       }
-      const int s = gk % kKStages;
-      if (gk >= kKStages &&
-          !mbar_wait(&k_empty[s], ((gk / kKStages) + 1) & 1, a.err, abort_flag, tmo)) {
+      const int s = gk % kKS;
+      if (gk >= kKS &&
+          !mbar_wait(&k_empty[s], ((gk / kKS) + 1) & 1, a.err, abort_flag, tmo)) {
         ok = false;
         break;
       }
@@ -260,12 +261,13 @@ __device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, con
   }
   // Let every copy still in flight land before the CTA can exit.
   if (q_loads > 0) drain_wait(q_full, (q_loads - 1) & 1, a.err, tmo);
-  for (int g = max(0, gk - kKStages); g < gk; ++g)
-    drain_wait(&k_full[g % kKStages], (g / kKStages) & 1, a.err, tmo);
+  for (int g = max(0, gk - kKS); g < gk; ++g)
+    drain_wait(&k_full[g % kKS], (g / kKS) & 1, a.err, tmo);
 }
 
 // TMA producer of the value blocks V_j (one thread) into a kVStages-slot ring, released by
 // the commit after the P.V MMAs that read the slot (v_empty).
+template <int kVS>
 __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, const CUtensorMap* tmV,
                                           uint8_t* sV, uint64_t* v_full, uint64_t* v_empty,
                                           volatile int* abort_flag, uint64_t tmo) {
@@ -277,9 +279,9 @@ __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, cons
     for (int j = 0; j < it.L; ++j) {
       int kb = block_of(a, it, j);
       if (kb < 0 || kb > it.I) kb = it.I;
-      const int s = gv % kVStages;
-      if (gv >= kVStages &&
-          !mbar_wait(&v_empty[s], ((gv / kVStages) + 1) & 1, a.err, abort_flag, tmo)) {
+      const int s = gv % kVS;
+      if (gv >= kVS &&
+          !mbar_wait(&v_empty[s], ((gv / kVS) + 1) & 1, a.err, abort_flag, tmo)) {
         ok = false;
         break;
       }
@@ -291,8 +293,8 @@ __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, cons
       ++gv;
     }
   }
-  for (int g = max(0, gv - kVStages); g < gv; ++g)
-    drain_wait(&v_full[g % kVStages], (g / kVStages) & 1, a.err, tmo);
+  for (int g = max(0, gv - kVS); g < gv; ++g)
+    drain_wait(&v_full[g % kVS], (g / kVS) & 1, a.err, tmo);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -362,9 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kRescueLoaderRegs>();
   if (warp == 8) {
     if (lane == 0)
-      produce_qk(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full, k_empty, abort_flag, tmo);
+      produce_qk<kKStages>(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full, k_empty,
+                           abort_flag, tmo);
   } else if (warp == 10) {
-    if (lane == 0) produce_v(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
+    if (lane == 0) produce_v<kVStages>(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -584,38 +587,45 @@ constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 384;
 constexpr float kOverflowSum = 18446744073709551616.0f;  // 2^64
 constexpr size_t kXBytes = 2 * 2 * kBlk * sizeof(float) + 16;  // row max, row sum per tile; flag
-constexpr size_t kSmemFast = 1024 + kTileBytes * (1 + kKStages + kVStages) + kXBytes + 512;
+// Deeper K and V rings than the rescue pass: the dynamic shared memory must then start on
+// a 1024-byte boundary (the 128-byte swizzle atoms), which the kernel checks instead of
+// padding.
+constexpr int kFastKStages = 4;
+constexpr int kFastVStages = 2;
+constexpr size_t kSmemFast = kTileBytes * (1 + kFastKStages + kFastVStages) + kXBytes + 256;
 
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrRange);
+    return;
+  }
+  uint8_t* sQ = smem_raw;
   uint8_t* sK = sQ + kTileBytes;
-  uint8_t* sV = sK + kKStages * kTileBytes;
-  float* sXM = reinterpret_cast<float*>(sV + kVStages * kTileBytes);  // [tile][row] first-block max
+  uint8_t* sV = sK + kFastKStages * kTileBytes;
+  float* sXM = reinterpret_cast<float*>(sV + kFastVStages * kTileBytes);  // [tile][row] first-block max
   float* sXL = sXM + 2 * kBlk;                                         // [tile][row] row sum
   volatile int* sRedo = reinterpret_cast<volatile int*>(sXL + 2 * kBlk);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sXM) + kXBytes);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;    // [3]
-  uint64_t* k_empty = bars + 5;   // [3]
-  uint64_t* v_full = bars + 8;    // [2]
-  uint64_t* v_empty = bars + 10;  // [2]
-  uint64_t* s_full = bars + 12;   // [2] S_t holds the tile's next block
-  uint64_t* s_free = bars + 14;   // [2] the tile's softmax has loaded S_t
-  uint64_t* p_full = bars + 16;   // [2] P_t written
-  uint64_t* p_free = bars + 18;   // [2] the P.V MMAs reading P_t have completed
-  uint64_t* o_done = bars + 20;
-  uint64_t* o_free = bars + 21;
-  uint64_t* x_ready = bars + 22;  // both tiles' first-block maxima are in sXM
-  uint64_t* l_ready = bars + 23;  // both tiles' row sums are in sXL
-  uint64_t* drain = bars + 24;    // [2] one per MMA-issuing thread
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+  uint64_t* k_full = bars + 2;                   // [kFastKStages]
+  uint64_t* k_empty = k_full + kFastKStages;     // [kFastKStages]
+  uint64_t* v_full = k_empty + kFastKStages;     // [kFastVStages]
+  uint64_t* v_empty = v_full + kFastVStages;     // [kFastVStages]
+  uint64_t* s_full = v_empty + kFastVStages;     // [2] S_t holds the tile's next block
+  uint64_t* s_free = s_full + 2;                 // [2] the tile's softmax has loaded S_t
+  uint64_t* p_full = s_free + 2;                 // [2] P_t written
+  uint64_t* p_free = p_full + 2;                 // [2] the P.V MMAs reading P_t have completed
+  uint64_t* o_done = p_free + 2;
+  uint64_t* o_free = o_done + 1;
+  uint64_t* x_ready = o_free + 1;                // both tiles' first-block maxima are in sXM
+  uint64_t* l_ready = x_ready + 1;               // both tiles' row sums are in sXL
+  uint64_t* drain = l_ready + 1;                 // [2] one per MMA-issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -625,11 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kKStages; ++s) {
+    for (int s = 0; s < kFastKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
+    for (int s = 0; s < kFastVStages; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -661,10 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kLoaderRegs>();
     if (warp == 8) {
       if (lane == 0)
-        produce_qk(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full, k_empty, abort_flag,
-                   tmo);
+        produce_qk<kFastKStages>(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full,
+                                 k_empty, abort_flag, tmo);
     } else if (warp == 10) {
-      if (lane == 0) produce_v(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
+      if (lane == 0)
+        produce_v<kFastVStages>(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
     } else if (warp == 9) {
       // ---------------------------------------------------------------- S issuer
       // S_j = Q K_j^T into tile (j & 1)'s buffer, as soon as the tile's softmax has loaded
@@ -684,9 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int j = 0; j < it.L; ++j) {
             const int t = j & 1;
-            const int s = gk % kKStages;
+            const int s = gk % kFastKStages;
             if ((ns[t] > 0 && !mbar_wait(&s_free[t], (ns[t] - 1) & 1, a.err, abort_flag, tmo)) ||
-                !mbar_wait(&k_full[s], (gk / kKStages) & 1, a.err, abort_flag, tmo)) {
+                !mbar_wait(&k_full[s], (gk / kFastKStages) & 1, a.err, abort_flag, tmo)) {
               ok = false;
               break;
             }
@@ -721,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Item it = get_item(a, k, gridDim.x, num_items);
           for (int j = 0; j < it.L; ++j) {
             const int t = j & 1;
-            const int s = gv % kVStages;
+            const int s = gv % kFastVStages;
             if (!mbar_wait(&p_full[t], np[t] & 1, a.err, abort_flag, tmo) ||
                 (j == 0 && item_idx > 0 &&
                  !mbar_wait(o_free, (item_idx - 1) & 1, a.err, abort_flag, tmo)) ||
-                !mbar_wait(&v_full[s], (gv / kVStages) & 1, a.err, abort_flag, tmo)) {
+                !mbar_wait(&v_full[s], (gv / kFastVStages) & 1, a.err, abort_flag, tmo)) {
               ok = false;
               break;
             }
@@ -767,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&s_full[t], ns & 1, a.err, abort_flag, tmo)) return false;
       ++ns;
       tc_fence_after();
-      if (q == 0 && lane == 0) mbar_arrive(&k_empty[(gbase + jj) % kKStages]);
+      if (q == 0 && lane == 0) mbar_arrive(&k_empty[(gbase + jj) % kFastKStages]);
       tmem_ld128(s_addr, v);
       tc_fence_before();
       __syncwarp();
