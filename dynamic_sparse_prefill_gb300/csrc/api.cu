@@ -78,6 +78,26 @@ crisp_status make_map(crisp_ctx ctx, CUtensorMap* map, const void* base, int64_t
   return CRISP_OK;
 }
 
+// The attention kernels' map: the same [rows][128] bf16 tensor seen as {64 columns, rows,
+// 2 column halves} (strides 256 B and 128 B), box {64, 128, 2}: one copy per 128 x 128
+// tile, landing in the two-region swizzled layout (see ptx.cuh).
+crisp_status make_map3(crisp_ctx ctx, CUtensorMap* map, const void* base, int64_t rows) {
+  cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(rows), 2};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(kD) * 2, 128};
+  cuuint32_t box[3] = {64, 128, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                           gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(ctx->last_err, sizeof(ctx->last_err), "cuTensorMapEncodeTiled (3-D) failed (%d)",
+             static_cast<int>(r));
+    return CRISP_ERR_CUDA;
+  }
+  return CRISP_OK;
+}
+
 crisp_status launched(crisp_ctx ctx, cudaError_t e, const char* what) {
   if (e == cudaSuccess) return CRISP_OK;
   set_err(ctx, what, e);
@@ -292,9 +312,9 @@ static crisp_status run_attention(crisp_ctx ctx, const crisp_dims* dims, const v
   if (!dense && (!ctx->has_sel || !same_dims(ctx->sel_dims, *dims))) return CRISP_ERR_NO_SELECTION;
   const Shape s = make_shape(*dims);
   CUtensorMap tmQ, tmK, tmV;
-  if ((st = make_map(ctx, &tmQ, Q, static_cast<int64_t>(s.H) * s.n)) != CRISP_OK) return st;
-  if ((st = make_map(ctx, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
-  if ((st = make_map(ctx, &tmV, V, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
+  if ((st = make_map3(ctx, &tmQ, Q, static_cast<int64_t>(s.H) * s.n)) != CRISP_OK) return st;
+  if ((st = make_map3(ctx, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
+  if ((st = make_map3(ctx, &tmV, V, static_cast<int64_t>(s.Hkv) * s.n)) != CRISP_OK) return st;
   return launched(ctx,
                   launch_attention(ctx, s, tmQ, tmK, tmV, O, dense, static_cast<cudaStream_t>(stream)),
                   "attention");

@@ -236,8 +236,7 @@ __device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, con
     }
     const int qrow = it.h * a.n + it.I * kBlk;
     mbar_arrive_expect_tx(q_full, kTileBytes);
-    tma_load_2d(sQ, tmQ, q_full, 0, qrow);
-    tma_load_2d(sQ + kTileBytes / 2, tmQ, q_full, 64, qrow);
+    tma_load_3d(sQ, tmQ, q_full, 0, qrow, 0);
     ++q_loads;
     for (int j = 0; j < it.L; ++j) {
       int kb = block_of(a, it, j);
@@ -254,8 +253,7 @@ __device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, con
       uint8_t* dst = sK + s * kTileBytes;
       const int row = it.hk * a.n + kb * kBlk;
       mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-      tma_load_2d(dst, tmK, &k_full[s], 0, row);
-      tma_load_2d(dst + kTileBytes / 2, tmK, &k_full[s], 64, row);
+      tma_load_3d(dst, tmK, &k_full[s], 0, row, 0);
       ++gk;
     }
   }
@@ -265,8 +263,9 @@ __device__ __forceinline__ void produce_qk(const AttnArgs& a, int num_items, con
     drain_wait(&k_full[g % kKS], (g / kKS) & 1, a.err, tmo);
 }
 
-// TMA producer of the value blocks V_j (one thread) into a kVStages-slot ring, released by
-// the commit after the P.V MMAs that read the slot (v_empty).
+// TMA producer of the value blocks V_j (one thread) into a kVS-slot ring, released by the
+// commit after the P.V MMAs that read the slot (v_empty).  Both producers load each tile
+// with one 3-D copy (see tma_load_3d).
 template <int kVS>
 __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, const CUtensorMap* tmV,
                                           uint8_t* sV, uint64_t* v_full, uint64_t* v_empty,
@@ -288,8 +287,7 @@ __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, cons
       uint8_t* dst = sV + s * kTileBytes;
       const int row = it.hk * a.n + kb * kBlk;
       mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-      tma_load_2d(dst, tmV, &v_full[s], 0, row);
-      tma_load_2d(dst + kTileBytes / 2, tmV, &v_full[s], 64, row);
+      tma_load_3d(dst, tmV, &v_full[s], 0, row, 0);
       ++gv;
     }
   }
@@ -592,6 +590,10 @@ constexpr size_t kXBytes = 2 * 2 * kBlk * sizeof(float) + 16;  // row max, row s
 // padding.
 constexpr int kFastKStages = 4;
 constexpr int kFastVStages = 2;
+// Blocks alternate between the tiles by their CTA-wide index g (g & 1), so a tile's previous
+// block is always g - 2 and the V slot of block g is P_t's slot too: one commit after P.V
+// (v_empty[g & 1]) frees both the V slot and the P buffer.
+static_assert(kFastVStages == 2, "v_empty doubles as the P buffers' release");
 constexpr size_t kSmemFast = kTileBytes * (1 + kFastKStages + kFastVStages) + kXBytes + 256;
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -619,8 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + kFastVStages;     // [2] S_t holds the tile's next block
   uint64_t* s_free = s_full + 2;                 // [2] the tile's softmax has loaded S_t
   uint64_t* p_full = s_free + 2;                 // [2] P_t written
-  uint64_t* p_free = p_full + 2;                 // [2] the P.V MMAs reading P_t have completed
-  uint64_t* o_done = p_free + 2;
+  uint64_t* o_done = p_full + 2;
   uint64_t* o_free = o_done + 1;
   uint64_t* x_ready = o_free + 1;                // both tiles' first-block maxima are in sXM
   uint64_t* l_ready = x_ready + 1;               // both tiles' row sums are in sXL
@@ -647,7 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&s_free[t], 4);   // one arrive per warp of the tile
       mbar_init(&p_full[t], 4);
-      mbar_init(&p_free[t], 1);
     }
     mbar_init(o_done, 1);
     mbar_init(o_free, 8);       // one arrive per softmax warp
@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           for (int j = 0; j < it.L; ++j) {
-            const int t = j & 1;
+            const int t = gk & 1;
             const int s = gk % kFastKStages;
             if ((ns[t] > 0 && !mbar_wait(&s_free[t], (ns[t] - 1) & 1, a.err, abort_flag, tmo)) ||
                 !mbar_wait(&k_full[s], (gk / kFastKStages) & 1, a.err, abort_flag, tmo)) {
@@ -731,8 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
           const Item it = get_item(a, k, gridDim.x, num_items);
           for (int j = 0; j < it.L; ++j) {
-            const int t = j & 1;
-            const int s = gv % kFastVStages;
+            const int t = gv & 1;
+            const int s = gv % kFastVStages;  // == t
             if (!mbar_wait(&p_full[t], np[t] & 1, a.err, abort_flag, tmo) ||
                 (j == 0 && item_idx > 0 &&
                  !mbar_wait(o_free, (item_idx - 1) & 1, a.err, abort_flag, tmo)) ||
@@ -750,7 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 1; kk < 8; ++kk)
               umma_bf16_tmem_a(tmem + kColO, p + kk * 8, dV + ((kk * 2048) >> 4), kIdescPV, 1u);
             umma_commit(&v_empty[s]);
-            umma_commit(&p_free[t]);
             ++np[t];
             ++gv;
           }
@@ -769,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + t * 128;
     const uint32_t p_addr = tmem + lane_off + kColP + t * 64;
-    int ns = 0, npw = 0, item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
+    int ns = 0, item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
     bool ok = true;
     uint32_t v[128];
     // Waits for the tile's next S block, loads it, hands the S buffer back to the MMA warp
@@ -787,14 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
       const Item it = get_item(a, k, gridDim.x, num_items);
+      const int j0 = (t ^ gbase) & 1;  // this tile's first block: (gbase + j0) & 1 == t
       // Row reference: the larger of the two tiles' first-block row maxima.
       float mfirst = -FLT_MAX;
-      if (t < it.L) {
-        if (!load_s(t)) {
+      if (j0 < it.L) {
+        if (!load_s(j0)) {
           ok = false;
           break;
         }
-        mfirst = (block_of(a, it, t) == it.I ? row_max<true>(v, r) : row_max<false>(v, r)) *
+        mfirst = (block_of(a, it, j0) == it.I ? row_max<true>(v, r) : row_max<false>(v, r)) *
                  a.scale_log2;
       }
       sXM[t * kBlk + r] = mfirst;
@@ -807,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float M = fmaxf(sXM[r], sXM[kBlk + r]);
       float l = 0.f;
       bool ovf = false;
-      for (int jj = t; jj < it.L; jj += 2) {
-        if (jj != t && !load_s(jj)) {
+      for (int jj = j0; jj < it.L; jj += 2) {
+        if (jj != j0 && !load_s(jj)) {
           ok = false;
           break;
         }
@@ -816,7 +816,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      : exp_pack<false>(v, a.scale_log2, M, r);
         ovf |= !(rs <= kOverflowSum);
         l += rs;
-        if (npw > 0 && !warp_wait(&p_free[t], (npw - 1) & 1, a.err, abort_flag, tmo)) {
+        // P_t last held block g - 2: wait for its P.V group (v_empty[t] completes once per
+        // group of the blocks g' with g' & 1 == t, block g' completing phase g' / 2).
+        const int g = gbase + jj;
+        if (g >= 2 && !warp_wait(&v_empty[t], ((g - 2) >> 1) & 1, a.err, abort_flag, tmo)) {
           ok = false;
           break;
         }
@@ -828,7 +831,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                           item_idx == 0 && jj + 2 >= it.L;
         __syncwarp();
         if (!drop && lane == 0) mbar_arrive(&p_full[t]);
-        ++npw;
       }
       gbase += it.L;
       if (!ok) break;

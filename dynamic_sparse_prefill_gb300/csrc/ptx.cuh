@@ -3,8 +3,9 @@
 // stores), plus the shared-memory and instruction descriptors the MMAs take.
 //
 // Operand layout used throughout: a 128-row bf16 tile with 128 columns is stored as two
-// "regions" of 128 rows x 64 columns (128 bytes per row), each written by one TMA box
-// with 128-byte swizzling: inside every 8-row / 1024-byte atom, the 16-byte chunk c of
+// "regions" of 128 rows x 64 columns (128 bytes per row), written by TMA with 128-byte
+// swizzling (one 2-D box per region, or one 3-D box for both): inside every 8-row /
+// 1024-byte atom, the 16-byte chunk c of
 // row r sits at chunk position c ^ (r % 8).  Regions start on 1024-byte boundaries.
 #pragma once
 #include <cstdint>
@@ -97,6 +98,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// 3-D tiled load: with a map of dims {64 columns, rows, 2 column halves} (strides 256 B and
+// 128 B) and box {64, 128, 2}, one copy lands a 128 x 128 bf16 tile in the two-region
+// 128-byte-swizzled layout described at the top of this file.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 
