@@ -684,8 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+        // Block g goes to tile g & 1; the tile's previous block is g - 2, so its buffer and
+        // barrier phases follow from g alone (phase of block g: (g >> 1) & 1).
         int gk = 0, item_idx = 0;
-        int ns[2] = {0, 0};  // S blocks issued into S_t so far
         bool ok = true;
         for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
           const Item it = get_item(a, k, gridDim.x, num_items);
@@ -696,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < it.L; ++j) {
             const int t = gk & 1;
             const int s = gk % kFastKStages;
-            if ((ns[t] > 0 && !mbar_wait(&s_free[t], (ns[t] - 1) & 1, a.err, abort_flag, tmo)) ||
+            if ((gk >= 2 && !mbar_wait(&s_free[t], ((gk - 2) >> 1) & 1, a.err, abort_flag, tmo)) ||
                 !mbar_wait(&k_full[s], (gk / kFastKStages) & 1, a.err, abort_flag, tmo)) {
               ok = false;
               break;
@@ -712,7 +713,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(&s_full[t]);
             if (j == it.L - 1) umma_commit(q_empty);
-            ++ns[t];
             ++gk;
           }
         }
@@ -726,14 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint64_t dV0 = sdesc_sw128(smem_u32(sV), kTileBytes / 2, 1024);
         int gv = 0, item_idx = 0;
-        int np[2] = {0, 0};  // P.V groups issued from P_t so far
         bool ok = true;
         for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
           const Item it = get_item(a, k, gridDim.x, num_items);
           for (int j = 0; j < it.L; ++j) {
             const int t = gv & 1;
             const int s = gv % kFastVStages;  // == t
-            if (!mbar_wait(&p_full[t], np[t] & 1, a.err, abort_flag, tmo) ||
+            if (!mbar_wait(&p_full[t], (gv >> 1) & 1, a.err, abort_flag, tmo) ||
                 (j == 0 && item_idx > 0 &&
                  !mbar_wait(o_free, (item_idx - 1) & 1, a.err, abort_flag, tmo)) ||
                 !mbar_wait(&v_full[s], (gv / kFastVStages) & 1, a.err, abort_flag, tmo)) {
@@ -750,7 +749,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 1; kk < 8; ++kk)
               umma_bf16_tmem_a(tmem + kColO, p + kk * 8, dV + ((kk * 2048) >> 4), kIdescPV, 1u);
             umma_commit(&v_empty[s]);
-            ++np[t];
             ++gv;
           }
           if (ok) umma_commit(o_done);
@@ -768,14 +766,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + t * 128;
     const uint32_t p_addr = tmem + lane_off + kColP + t * 64;
-    int ns = 0, item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
+    int item_idx = 0, gbase = 0;  // gbase: CTA-wide index of the item's first block
     bool ok = true;
     uint32_t v[128];
     // Waits for the tile's next S block, loads it, hands the S buffer back to the MMA warp
     // and releases K_j's ring slot (S_j complete means K_j has been read).
     auto load_s = [&](int jj) -> bool {
-      if (!warp_wait(&s_full[t], ns & 1, a.err, abort_flag, tmo)) return false;
-      ++ns;
+      if (!warp_wait(&s_full[t], ((gbase + jj) >> 1) & 1, a.err, abort_flag, tmo)) return false;
       tc_fence_after();
       if (q == 0 && lane == 0) mbar_arrive(&k_empty[(gbase + jj) % kFastKStages]);
       tmem_ld128(s_addr, v);
