@@ -320,24 +320,23 @@ def run_gpu(args, w, rank, world):
         if ctx.sync_status() != 0:
             raise RuntimeError("device error in dense attention")
 
-    # end to end through the public API with host buffers (pinned), copies included
+    # end to end through the public API with host buffers (pinned), copies included:
+    # crisp_prefill_host uploads, computes and downloads chunk by chunk, overlapped
     qh = torch.from_numpy(g["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
     kh = torch.from_numpy(g["k"].view(np.int16)).view(torch.bfloat16).pin_memory()
     vh = torch.from_numpy(g["v"].view(np.int16)).view(torch.bfloat16).pin_memory()
     oh = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(1, min(args.steps, 3))
-    ctx.prefill(dims, q, k, v, cfg, o)
+    ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q, k, v, o)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
-        v.copy_(vh, non_blocking=True)
-        ctx.prefill(dims, q, k, v, cfg, o)
-        oh.copy_(o, non_blocking=True)
+        ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q, k, v, o)
     e1.record(stream)
     torch.cuda.synchronize()
+    if ctx.sync_status() != 0:
+        raise RuntimeError("device error in the end-to-end run")
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = int(qh.numel() + kh.numel() + vh.numel()) * 2
     d2h = int(oh.numel()) * 2

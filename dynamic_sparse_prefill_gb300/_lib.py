@@ -27,7 +27,7 @@ EXPORTED = ["crisp_cfg_default", "crisp_create", "crisp_destroy", "crisp_select"
             "crisp_prefill", "crisp_dense", "crisp_selection_get", "crisp_selection_set",
             "crisp_selection_stats", "crisp_sync_status", "crisp_set_debug",
             "crisp_status_string", "crisp_last_error", "crisp_route_static", "crisp_jsd",
-            "crisp_attend_info"]
+            "crisp_attend_info", "crisp_prefill_host"]
 
 
 class Dims(ctypes.Structure):
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "crisp_selection_set": (ctypes.c_int, [P, DP, P, P, P, ctypes.c_int64]),
         "crisp_selection_stats": (ctypes.c_int, [P, DP, P, ctypes.POINTER(Stats)]),
         "crisp_attend_info": (ctypes.c_int, [P, P, ctypes.POINTER(ctypes.c_int64)]),
+        "crisp_prefill_host": (ctypes.c_int, [P, DP, P, P, P, CP, P, P, P, P, P, P]),
         "crisp_sync_status": (ctypes.c_int, [P, P]),
         "crisp_set_debug": (ctypes.c_int, [P, ctypes.c_uint32, ctypes.c_uint64]),
         "crisp_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -165,6 +166,14 @@ class Context:
         self._check(self._lib.crisp_prefill(self._h, ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v),
                                             ctypes.byref(cfg), _ptr(o), _stream(stream)),
                     "crisp_prefill")
+
+    def prefill_host(self, dims, qh, kh, vh, cfg, oh, q, k, v, o, stream=None):
+        """crisp_prefill from (page-locked) host tensors qh, kh, vh into oh, staged through
+        the device tensors q, k, v, o with the copies overlapping the work."""
+        self._check(self._lib.crisp_prefill_host(self._h, ctypes.byref(dims), _ptr(qh), _ptr(kh),
+                                                 _ptr(vh), ctypes.byref(cfg), _ptr(oh), _ptr(q),
+                                                 _ptr(k), _ptr(v), _ptr(o), _stream(stream)),
+                    "crisp_prefill_host")
 
     def dense(self, dims, q, k, v, o, stream=None):
         self._check(self._lib.crisp_dense(self._h, ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v),

@@ -8,6 +8,8 @@
 #include <cstring>
 #include <vector>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -112,6 +114,32 @@ crisp_status check_common(crisp_ctx ctx, const crisp_dims* dims) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != ctx->device) return CRISP_ERR_INVALID_ARG;
   return CRISP_OK;
+}
+
+bool create_copy_streams(crisp_ctx ctx) {
+  const unsigned f = cudaEventDisableTiming;
+  if (cudaStreamCreateWithFlags(&ctx->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ctx->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->ev_entry, f) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ctx->ev_done, f) != cudaSuccess)
+    return false;
+  for (int c = 0; c < crisp_ctx_s::kMaxChunks; ++c)
+    if (cudaEventCreateWithFlags(&ctx->ev_in[c], f) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_out[c], f) != cudaSuccess)
+      return false;
+  return true;
+}
+
+void destroy_copy_streams(crisp_ctx ctx) {
+  for (int c = 0; c < crisp_ctx_s::kMaxChunks; ++c) {
+    if (ctx->ev_in[c]) cudaEventDestroy(ctx->ev_in[c]);
+    if (ctx->ev_out[c]) cudaEventDestroy(ctx->ev_out[c]);
+  }
+  if (ctx->ev_entry) cudaEventDestroy(ctx->ev_entry);
+  if (ctx->ev_done) cudaEventDestroy(ctx->ev_done);
+  if (ctx->h2d) cudaStreamDestroy(ctx->h2d);
+  if (ctx->d2h) cudaStreamDestroy(ctx->d2h);
+  cudaGetLastError();
 }
 
 }  // namespace
@@ -258,7 +286,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
     off += (pc.bytes + 255) & ~static_cast<size_t>(255);
   }
   if (cudaMemset(w.err, 0, sizeof(uint32_t)) != cudaSuccess ||
-      cudaMemset(w.redo_count, 0, sizeof(int)) != cudaSuccess) {
+      cudaMemset(w.redo_count, 0, sizeof(int)) != cudaSuccess || !create_copy_streams(ctx)) {
+    destroy_copy_streams(ctx);
     cudaFree(base);
     delete ctx;
     return CRISP_ERR_CUDA;
@@ -270,6 +299,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
 void crisp_destroy(crisp_ctx ctx) {
   if (!ctx) return;
   cudaDeviceSynchronize();
+  destroy_copy_streams(ctx);
   cudaFree(ctx->ws.st_m);  // the first piece is the allocation's base
   delete ctx;
 }
@@ -336,6 +366,69 @@ crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q,
   crisp_status st = crisp_select(ctx, dims, Q, K, cfg, stream);
   if (st != CRISP_OK) return st;
   return crisp_attend(ctx, dims, Q, K, V, O, stream);
+}
+
+crisp_status crisp_prefill_host(crisp_ctx ctx, const crisp_dims* dims, const void* Q_host,
+                                const void* K_host, const void* V_host, const crisp_cfg* cfg,
+                                void* O_host, void* Q, void* K, void* V, void* O, void* stream) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if ((st = check_cfg(cfg)) != CRISP_OK) return st;
+  if (!Q_host || !K_host || !V_host || !O_host || !Q || !K || !V || !O || !aligned16(Q) ||
+      !aligned16(K) || !aligned16(V) || !aligned16(O))
+    return CRISP_ERR_INVALID_ARG;
+  const Shape s = make_shape(*dims);
+  const int group = s.group;
+  // KV heads per chunk: at least 8 query-block rows per SM in every chunk, and no more
+  // than kMaxChunks chunks.
+  const int rows_per_kv = group * s.nb;
+  int per = (8 * ctx->num_sms + rows_per_kv - 1) / rows_per_kv;
+  per = std::max(per, (s.Hkv + crisp_ctx_s::kMaxChunks - 1) / crisp_ctx_s::kMaxChunks);
+  per = std::max(1, std::min(per, s.Hkv));
+  const int nchunks = (s.Hkv + per - 1) / per;
+  const size_t head_bytes = static_cast<size_t>(s.n) * kD * 2;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  auto ok = [&](cudaError_t e, const char* what) { return launched(ctx, e, what) == CRISP_OK; };
+  // Work already queued on the caller's stream (earlier use of Q/K/V/O) comes first.
+  if (!ok(cudaEventRecord(ctx->ev_entry, cs), "record") ||
+      !ok(cudaStreamWaitEvent(ctx->h2d, ctx->ev_entry, 0), "wait") ||
+      !ok(cudaStreamWaitEvent(ctx->d2h, ctx->ev_entry, 0), "wait"))
+    return CRISP_ERR_CUDA;
+  for (int c = 0; c < nchunks; ++c) {
+    const int g0 = c * per, m = std::min(per, s.Hkv - g0), h0 = g0 * group;
+    const size_t qoff = static_cast<size_t>(h0) * head_bytes, kvoff = static_cast<size_t>(g0) * head_bytes;
+    const size_t qbytes = static_cast<size_t>(m) * group * head_bytes, kvbytes = static_cast<size_t>(m) * head_bytes;
+    // upload chunk c (the copy stream runs ahead of the compute stream)
+    if (!ok(cudaMemcpyAsync(static_cast<char*>(Q) + qoff, static_cast<const char*>(Q_host) + qoff,
+                            qbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload Q") ||
+        !ok(cudaMemcpyAsync(static_cast<char*>(K) + kvoff, static_cast<const char*>(K_host) + kvoff,
+                            kvbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload K") ||
+        !ok(cudaMemcpyAsync(static_cast<char*>(V) + kvoff, static_cast<const char*>(V_host) + kvoff,
+                            kvbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload V") ||
+        !ok(cudaEventRecord(ctx->ev_in[c], ctx->h2d), "record") ||
+        !ok(cudaStreamWaitEvent(cs, ctx->ev_in[c], 0), "wait"))
+      return CRISP_ERR_CUDA;
+    // select and attend chunk c: an independent problem of m KV heads
+    const crisp_dims sub{1, s.n, m * group, m, kD};
+    if ((st = crisp_select(ctx, &sub, static_cast<char*>(Q) + qoff, static_cast<char*>(K) + kvoff,
+                           cfg, stream)) != CRISP_OK ||
+        (st = crisp_attend(ctx, &sub, static_cast<char*>(Q) + qoff, static_cast<char*>(K) + kvoff,
+                           static_cast<char*>(V) + kvoff, static_cast<char*>(O) + qoff, stream)) !=
+            CRISP_OK)
+      return st;
+    // download chunk c's output once it is written
+    if (!ok(cudaEventRecord(ctx->ev_out[c], cs), "record") ||
+        !ok(cudaStreamWaitEvent(ctx->d2h, ctx->ev_out[c], 0), "wait") ||
+        !ok(cudaMemcpyAsync(static_cast<char*>(O_host) + qoff, static_cast<char*>(O) + qoff, qbytes,
+                            cudaMemcpyDeviceToHost, ctx->d2h), "download O"))
+      return CRISP_ERR_CUDA;
+  }
+  if (!ok(cudaEventRecord(ctx->ev_done, ctx->d2h), "record") ||
+      !ok(cudaStreamWaitEvent(cs, ctx->ev_done, 0), "wait"))
+    return CRISP_ERR_CUDA;
+  ctx->has_sel = false;  // the context held one chunk's selection at a time
+  ctx->has_patsearch = false;
+  return CRISP_OK;
 }
 
 static crisp_status copy_out(crisp_ctx ctx, void* dst, const void* src, size_t bytes) {

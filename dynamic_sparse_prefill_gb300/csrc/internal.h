@@ -90,6 +90,12 @@ struct crisp_ctx_s {
   crisp_dims sel_dims{};
   uint32_t debug_flags = 0;
   uint64_t timeout_ns = 1000000000ull;
+  // crisp_prefill_host: copy streams and the events that order them against the caller's
+  // stream (created with the context).
+  static constexpr int kMaxChunks = 64;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_in[kMaxChunks] = {}, ev_out[kMaxChunks] = {};
   char last_err[256] = {0};
 };
 

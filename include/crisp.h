@@ -120,6 +120,22 @@ crisp_status crisp_attend(crisp_ctx ctx, const crisp_dims* dims, const void* Q, 
 crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
                            const void* V, const crisp_cfg* cfg, void* O, void* stream);
 
+/* crisp_prefill from host memory, overlapping the copies with the work: the heads are
+ * independent ("Method step details" runs steps 1-4 per head), so the call splits them
+ * into chunks of whole KV-head groups and, per chunk, uploads Q, K, V (host -> the
+ * caller's device buffers Q, K, V), selects and attends on `stream`, and downloads O
+ * (-> O_host) while the next chunk is uploaded and computed.  Two copy streams owned by
+ * the context carry the copies; events order them against `stream`, so synchronising
+ * `stream` waits for everything, O_host included.  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to overlap.  All eight buffers are
+ * caller-owned and hold the full [batch*heads][n][128] tensors; the call allocates
+ * nothing.  Leaves the context without a selection (crisp_attend then returns
+ * CRISP_ERR_NO_SELECTION until the next crisp_select); crisp_attend_info reports the
+ * last chunk. */
+crisp_status crisp_prefill_host(crisp_ctx ctx, const crisp_dims* dims, const void* Q_host,
+                                const void* K_host, const void* V_host, const crisp_cfg* cfg,
+                                void* O_host, void* Q, void* K, void* V, void* O, void* stream);
+
 /* Dense causal attention with the same kernel and every key block K <= I: the in-library
  * denominator of the speedup ("Prerequisites", FlashAttention).  Writes O; does not touch
  * the selection. */

@@ -231,6 +231,35 @@ def test_rescue_pass_recomputes_overflowing_rows(dsp):
     ctx.close()
 
 
+@pytest.mark.parametrize("name", ["tiny_n4k", "llama8b_n32k"])
+def test_prefill_host_matches_device_path(dsp, name):
+    """crisp_prefill_host (host buffers, chunked by KV-head groups, copies overlapped)
+    gives the device path's output: the heads are independent, so per-chunk selection and
+    attention are the same computation (up to the attention's summation order)."""
+    w = get(name)
+    g = generate(w)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    cfg = _cfg(dsp, w)
+    o = torch.empty_like(q)
+    ctx.prefill(dims, q, k, v, cfg, o)
+    assert ctx.sync_status() == 0
+    ref = o.float().cpu().numpy().astype(np.float64)
+    t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = t(g["q"]), t(g["k"]), t(g["v"])
+    oh = torch.zeros(o.shape, dtype=torch.bfloat16).pin_memory()
+    q2, k2, v2, o2 = (torch.empty_like(x) for x in (q, k, v, o))
+    ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q2, k2, v2, o2)
+    assert ctx.sync_status() == 0
+    got = oh.float().numpy()
+    for h in range(w.hq):
+        compare_outputs(got[h], ref[h], f"prefill_host vs prefill, head {h}")
+    with pytest.raises(dsp.CrispError):   # the call leaves no selection behind
+        ctx.attend(dims, q, k, v, o)
+    ctx.close()
+
+
 def test_timeout_is_reported_and_context_recovers(dsp):
     """A dropped barrier arrive makes a bounded wait run out: the kernel exits, the host
     reads CRISP_ERR_TIMEOUT, and the next call on the same context succeeds."""
