@@ -34,10 +34,15 @@ METRIC = ("sparse prefill attn ms/layer and TFLOP/s at 128k/512k; speedup vs in-
 UNIT = "ms/layer"
 B = 128
 D = 128
-# Kernel launches of one crisp_prefill: PatSearch 4, PEIndex 16, CSR 4, work order 3,
-# attention 2 (the fast pass and the rescue pass, which returns at once when no row was
-# listed).
-LAUNCHES_PER_PREFILL = 29
+def launches_per_prefill(w, sms: int) -> int:
+    """Kernel launches of one crisp_prefill: PatSearch 4, PEIndex 16, CSR 4, work order 3,
+    then the fast attention kernel once per group of KV heads (each group holds at least 8
+    query-block rows per SM, the library's rule) and the rescue pass once (it returns at
+    once when no row was listed)."""
+    per_kv = (w.hq // w.hkv) * (w.n // B)
+    hkv = w.batch * w.hkv
+    per = min(max(-(-8 * sms // per_kv), 1), hkv)
+    return 27 + -(-hkv // per) + 1
 
 
 def algorithmic_flops(nnz: int, rows: int) -> float:
@@ -369,7 +374,7 @@ def run_gpu(args, w, rank, world):
                      "peak_kind": f"bf16 sustained, {peak_kind}",
                      "traffic": recorded_traffic(w.name),
                      "algorithmic_flops_per_launch": flops},
-        "gpu_launches": LAUNCHES_PER_PREFILL * args.steps,
+        "gpu_launches": launches_per_prefill(w, torch.cuda.get_device_properties(0).multi_processor_count) * args.steps,
         "e2e": {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),

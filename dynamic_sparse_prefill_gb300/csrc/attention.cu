@@ -149,6 +149,7 @@ __device__ __forceinline__ float exp_pack(uint32_t (&v)[128], float scale, float
 struct AttnArgs {
   int n, nb, H, hq, hkv, group;
   int num_items;
+  int item_base;  // the launch covers entries [item_base, item_base + num_items) of the order
   float scale_log2;
   const int64_t* row_ptr;  // CSR of the selection (sparse mode)
   const int32_t* col;
@@ -182,7 +183,7 @@ __device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G, int nu
   const int m = k / G, pos = k % G;
   const int base = m * G;
   const int wsize = min(G, num_items - base);
-  const int ke = (m & 1) ? base + wsize - 1 - pos : k;
+  const int ke = ((m & 1) ? base + wsize - 1 - pos : k) + a.item_base;
   Item it;
   if (a.list != nullptr) {
     const int row = a.list[ke];
@@ -926,6 +927,12 @@ __global__ void order_scatter_kernel(const int64_t* __restrict__ row_ptr, int ro
 
 }  // namespace
 
+int attention_kv_heads_per_launch(const Shape& s, int num_sms) {
+  const int per_kv = s.group * s.nb;
+  const int per = (8 * num_sms + per_kv - 1) / per_kv;
+  return per < 1 ? 1 : (per > s.Hkv ? s.Hkv : per);
+}
+
 cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& tmQ,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, void* O, bool dense,
                              cudaStream_t st) {
@@ -963,11 +970,23 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.redo_count = ctx->ws.redo_count;
   cudaError_t e = cudaMemsetAsync(ctx->ws.redo_count, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
-  const int grid = a.num_items < ctx->num_sms ? a.num_items : ctx->num_sms;
-  attention_kernel<<<grid, kThreads, kSmemFast, st>>>(tmQ, tmK, tmV, a);
+  // One launch per group of KV heads (the order is KV-head major and every KV head owns
+  // group * N_b rows): all CTAs of a launch then stream the same KV head's blocks, which
+  // keeps them in L2 (at 512k tokens, 3x less DRAM traffic than one launch over every
+  // head).  A group holds enough rows for 8 per SM.
+  const int per_kv = s.group * s.nb;
+  const int per = attention_kv_heads_per_launch(s, ctx->num_sms);
+  for (int g0 = 0; g0 < s.Hkv; g0 += per) {
+    const int m = min(per, s.Hkv - g0);
+    a.item_base = g0 * per_kv;
+    a.num_items = m * per_kv;
+    const int grid = a.num_items < ctx->num_sms ? a.num_items : ctx->num_sms;
+    attention_kernel<<<grid, kThreads, kSmemFast, st>>>(tmQ, tmK, tmV, a);
+  }
   // Rescue pass over the rows the fast pass listed (usually none: each CTA then reads the
   // count and returns).
   AttnArgs r = a;
+  r.item_base = 0;
   r.list = ctx->ws.redo;
   r.list_count = ctx->ws.redo_count;
   r.redo = nullptr;

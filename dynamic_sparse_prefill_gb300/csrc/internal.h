@@ -109,6 +109,8 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
 cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
                             const void* K, cudaStream_t st);
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st);
+// KV heads per launch of the fast attention kernel (launch_attention splits the heads).
+int attention_kv_heads_per_launch(const Shape& s, int num_sms);
 // tmQ/tmK/tmV: 3-D maps of Q, K, V (dims {64, rows, 2}, box {64, 128, 2}; see make_map3).
 cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& tmQ,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, void* O, bool dense,
