@@ -51,8 +51,9 @@ def algorithmic_flops(nnz: int, rows: int) -> float:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it
-    was taken on this workload with the current kernel source; else None."""
+    """DRAM bytes of one crisp_attend (summed over its attention-kernel launches) from the
+    committed ncu summary, if it was taken on this workload with the current kernel
+    source; else None."""
     import hashlib
     import re
     prof = os.path.join(ROOT, "profiles", f"attention_kernel_{workload}_traffic.md")
@@ -373,7 +374,9 @@ def run_gpu(args, w, rank, world):
                      "peak": peak, "unit": "TFLOP/s", "frac": att_tflops / peak,
                      "peak_kind": f"bf16 sustained, {peak_kind}",
                      "traffic": recorded_traffic(w.name),
-                     "algorithmic_flops_per_launch": flops},
+                     "unit_of_work": "one crisp_attend call (all launches of the attention "
+                                     "kernels for the layer)",
+                     "algorithmic_flops_per_attend": flops},
         "gpu_launches": launches_per_prefill(w, torch.cuda.get_device_properties(0).multi_processor_count) * args.steps,
         "e2e": {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
