@@ -245,6 +245,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.anc), sizeof(float) * H * 2 * kBlk},
       {reinterpret_cast<void**>(&w.rowM), sizeof(float) * H * kBlk},
       {reinterpret_cast<void**>(&w.rowZ), sizeof(float) * H * kBlk},
+      {reinterpret_cast<void**>(&w.row_part), sizeof(float2) * H * kRowSplit * kBlk},
+      {reinterpret_cast<void**>(&w.row_ticket), sizeof(int) * H},
       {reinterpret_cast<void**>(&w.pv), sizeof(float) * H * nb},
       {reinterpret_cast<void**>(&w.pshi), sizeof(float) * H * nb},
       {reinterpret_cast<void**>(&w.pslo), sizeof(float) * H * nb},
@@ -263,7 +265,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.pe), sizeof(PeState) * H},
       {reinterpret_cast<void**>(&w.eq_off), sizeof(int64_t) * H * (nb + 1)},
       {reinterpret_cast<void**>(&w.rowmask), sizeof(uint32_t) * H * nb * nbw},
-      {reinterpret_cast<void**>(&w.row_cnt), sizeof(int64_t) * H * nb},
+      {reinterpret_cast<void**>(&w.scan_blk), sizeof(int64_t) * ((H * nb + 1023) / 1024 + 1)},
       {reinterpret_cast<void**>(&w.row_ptr), sizeof(int64_t) * (H * nb + 1)},
       {reinterpret_cast<void**>(&w.col), sizeof(int32_t) * w.col_cap},
       {reinterpret_cast<void**>(&w.order), sizeof(int32_t) * H * nb},
@@ -286,7 +288,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
     off += (pc.bytes + 255) & ~static_cast<size_t>(255);
   }
   if (cudaMemset(w.err, 0, sizeof(uint32_t)) != cudaSuccess ||
-      cudaMemset(w.redo_count, 0, sizeof(int)) != cudaSuccess || !create_copy_streams(ctx)) {
+      cudaMemset(w.redo_count, 0, sizeof(int)) != cudaSuccess ||
+      cudaMemset(w.row_ticket, 0, sizeof(int) * H) != cudaSuccess || !create_copy_streams(ctx)) {
     destroy_copy_streams(ctx);
     cudaFree(base);
     delete ctx;

@@ -13,58 +13,105 @@
 namespace crisp {
 namespace {
 
-constexpr int kRowsPerCta = 16;
+constexpr int kRowsPerCta = 32;
 
+// Row masks of a VS head, one 32-key word per thread.  The vertical selection and the
+// slash selection reversed (bit x = sels[N_b-1-x]) are first packed into bit arrays in
+// shared memory; for query block I, key K <= I is a slash key iff sels[I-K], i.e. bit
+// N_b-1-I+K of the reversed array, so a row word is a 64-bit funnel shift of that array.
 __global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restrict__ route,
                                                          const uint8_t* __restrict__ selv,
                                                          const uint8_t* __restrict__ sels,
                                                          int nb, int nbw, uint32_t* rowmask) {
-  extern __shared__ uint8_t ssel[];
+  extern __shared__ uint32_t sbits[];  // [nbw] vertical, [nbw + 1] reversed slash
   const int h = blockIdx.y;
   if (!route[h]) return;
-  uint8_t* sv = ssel;
-  uint8_t* ss = ssel + nb;
-  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
-    sv[J] = selv[static_cast<size_t>(h) * nb + J];
-    ss[J] = sels[static_cast<size_t>(h) * nb + J];
-  }
-  __syncthreads();
+  uint32_t* sv = sbits;
+  uint32_t* sr = sbits + nbw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int I = blockIdx.x * kRowsPerCta + warp; I < min(nb, (blockIdx.x + 1) * kRowsPerCta);
-       I += 8) {
-    uint32_t* mrow = rowmask + (static_cast<size_t>(h) * nb + I) * nbw;
-    for (int wd = 0; wd < nbw; ++wd) {
-      const int K = wd * 32 + lane;
-      bool on = false;
-      if (K <= I) on = (K == 0) || (K == I) || sv[K] || ss[I - K];
-      const unsigned word = __ballot_sync(0xffffffffu, on);
-      if (lane == 0) mrow[wd] = word;
+  const uint8_t* v = selv + static_cast<size_t>(h) * nb;
+  const uint8_t* sl = sels + static_cast<size_t>(h) * nb;
+  for (int wd = warp; wd <= nbw; wd += 8) {
+    const int x = wd * 32 + lane;
+    const unsigned wv = __ballot_sync(0xffffffffu, wd < nbw && x < nb && v[x] != 0);
+    const unsigned ws = __ballot_sync(0xffffffffu, x < nb && sl[nb - 1 - x] != 0);
+    if (lane == 0) {
+      if (wd < nbw) sv[wd] = wv;
+      sr[wd] = ws;
     }
   }
+  __syncthreads();
+  const int I0 = blockIdx.x * kRowsPerCta;
+  const int nrows = min(kRowsPerCta, nb - I0);
+  for (int idx = threadIdx.x; idx < nrows * nbw; idx += blockDim.x) {
+    const int I = I0 + idx / nbw, wd = idx % nbw;
+    const int K0 = wd * 32;
+    uint32_t out = 0;
+    if (K0 <= I) {
+      const int sh = nb - 1 - I + K0;  // bit of the reversed array for K = K0 (<= nb - 1)
+      out = sv[wd] | __funnelshift_r(sr[sh >> 5], sr[(sh >> 5) + 1], sh & 31);
+      if (wd == 0) out |= 1u;  // the sink block
+      const int top = I - K0;  // bits 0..top are keys K <= I
+      if (top < 31) out &= (2u << top) - 1u;
+      if (top < 32) out |= 1u << top;  // the diagonal block
+    }
+    rowmask[(static_cast<size_t>(h) * nb + I) * nbw + wd] = out;
+  }
 }
 
-// row_cnt[row] = number of key blocks in the row's mask; a warp per row.
-__global__ void __launch_bounds__(256) csr_count_kernel(const uint32_t* __restrict__ rowmask,
-                                                        int64_t rows, int nbw, int64_t* row_cnt) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint32_t* m = rowmask + row * nbw;
-  int c = 0;
-  for (int wd = lane; wd < nbw; wd += 32) c += __popc(m[wd]);
+// Counts the blocks of 1024 rows (a warp per row) and scans them inside the CTA:
+// row_ptr[row] = offset within the CTA's rows, blk[b] = the CTA's total.
+__global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __restrict__ rowmask,
+                                                              int64_t rows, int nbw,
+                                                              int64_t* row_ptr, int64_t* blk) {
+  __shared__ int cnt[1024];
+  __shared__ int wsum[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 1024;
+  for (int i = warp; i < 1024; i += 32) {
+    const int64_t row = r0 + i;
+    int c = 0;
+    if (row < rows) {
+      const uint32_t* m = rowmask + row * nbw;
+      for (int wd = lane; wd < nbw; wd += 32) c += __popc(m[wd]);
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if (lane == 0) row_cnt[row] = c;
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) cnt[i] = c;
+  }
+  __syncthreads();
+  const int c = cnt[threadIdx.x];
+  int pre = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, pre, o);
+    if (lane >= o) pre += t;
+  }
+  if (lane == 31) wsum[warp] = pre;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int64_t row = r0 + threadIdx.x;
+  if (row < rows) row_ptr[row] = (warp > 0 ? wsum[warp - 1] : 0) + pre - c;
+  if (threadIdx.x == 1023) blk[blockIdx.x] = wsum[31];
 }
 
-// Exclusive scan of row_cnt into row_ptr (rows+1 entries) with one CTA.
-__global__ void __launch_bounds__(1024) csr_scan_kernel(const int64_t* __restrict__ row_cnt,
-                                                        int64_t rows, int64_t* row_ptr) {
+// Exclusive scan of the per-CTA totals (one CTA); row_ptr[rows] = nnz.
+__global__ void __launch_bounds__(1024) csr_blk_scan_kernel(int64_t* blk, int nblk, int64_t rows,
+                                                            int64_t* row_ptr) {
   __shared__ int64_t part[1024];
-  const int64_t per = (rows + 1023) / 1024;
-  const int64_t b0 = threadIdx.x * per, b1 = min(rows, b0 + per);
+  const int per = (nblk + 1023) / 1024;
+  const int b0 = threadIdx.x * per, b1 = min(nblk, b0 + per);
   int64_t s = 0;
-  for (int64_t i = b0; i < b1; ++i) s += row_cnt[i];
+  for (int i = b0; i < b1; ++i) s += blk[i];
   part[threadIdx.x] = s;
   __syncthreads();
   for (int off = 1; off < 1024; off <<= 1) {
@@ -74,38 +121,47 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const int64_t* __restric
     __syncthreads();
   }
   int64_t run = part[threadIdx.x] - s;
-  for (int64_t i = b0; i < b1; ++i) {
-    row_ptr[i] = run;
-    run += row_cnt[i];
+  for (int i = b0; i < b1; ++i) {
+    const int64_t c = blk[i];
+    blk[i] = run;
+    run += c;
   }
   if (threadIdx.x == 1023) row_ptr[rows] = part[1023];
 }
 
 // col[row_ptr[row] + k] = k-th set bit of the row's mask (ascending); a warp per row.
+// Finishes row_ptr (adds the CTA offset of the scan).  Lanes load 32 words at a time; then
+// the warp walks the nonzero ones, every lane writing the index of its bit if set, so each
+// word's entries are stored by consecutive lanes to consecutive addresses.
 __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restrict__ rowmask,
-                                                       const int64_t* __restrict__ row_ptr,
+                                                       int64_t* row_ptr,
+                                                       const int64_t* __restrict__ blk,
                                                        int64_t rows, int nbw, int32_t* col) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
+  int64_t off = row_ptr[row] + blk[row >> 10];
+  __syncwarp();
+  if (lane == 0) row_ptr[row] = off;
+  const uint32_t lt = (1u << lane) - 1u;
   const uint32_t* m = rowmask + row * nbw;
-  int64_t off = row_ptr[row];
   for (int wd0 = 0; wd0 < nbw; wd0 += 32) {
     const int wd = wd0 + lane;
-    uint32_t bits = wd < nbw ? m[wd] : 0u;
-    const int c = __popc(bits);
-    int pre = c;
+    const uint32_t bits = wd < nbw ? m[wd] : 0u;
+    int pre = __popc(bits);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(0xffffffffu, pre, o);
       if (lane >= o) pre += t;
     }
     const int total = __shfl_sync(0xffffffffu, pre, 31);
-    int64_t pos = off + pre - c;
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      col[pos++] = wd * 32 + b;
-      bits &= bits - 1;
+    unsigned nz = __ballot_sync(0xffffffffu, bits != 0u);
+    while (nz) {
+      const int src = __ffs(nz) - 1;
+      nz &= nz - 1u;
+      const uint32_t w = __shfl_sync(0xffffffffu, bits, src);
+      const int base = __shfl_sync(0xffffffffu, pre, src) - __popc(w);
+      if (w & (1u << lane)) col[off + base + __popc(w & lt)] = (wd0 + src) * 32 + lane;
     }
     off += total;
   }
@@ -115,13 +171,16 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
 
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st) {
   Workspace& w = ctx->ws;
-  vs_rowmask_kernel<<<dim3((s.nb + kRowsPerCta - 1) / kRowsPerCta, s.H), 256, 2 * s.nb, st>>>(
-      w.route, w.selv, w.sels, s.nb, s.nbw, w.rowmask);
+  vs_rowmask_kernel<<<dim3((s.nb + kRowsPerCta - 1) / kRowsPerCta, s.H), 256,
+                      sizeof(uint32_t) * (2 * s.nbw + 1), st>>>(w.route, w.selv, w.sels, s.nb,
+                                                                 s.nbw, w.rowmask);
   const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
-  csr_count_kernel<<<grid, 256, 0, st>>>(w.rowmask, rows, s.nbw, w.row_cnt);
-  csr_scan_kernel<<<1, 1024, 0, st>>>(w.row_cnt, rows, w.row_ptr);
-  csr_fill_kernel<<<grid, 256, 0, st>>>(w.rowmask, w.row_ptr, rows, s.nbw, w.col);
+  const int nblk = static_cast<int>((rows + 1023) / 1024);
+  csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.rowmask, rows, s.nbw, w.row_ptr, w.scan_blk);
+  csr_blk_scan_kernel<<<1, 1024, 0, st>>>(w.scan_blk, nblk, rows, w.row_ptr);
+  csr_fill_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(w.rowmask, w.row_ptr,
+                                                                        w.scan_blk, rows, s.nbw,
+                                                                        w.col);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,9 @@ struct PeState {
   unsigned long long count_eq;  // items equal to thresh
 };
 
+// CTAs per head that merge PatSearch's per-tile row statistics (patsearch.cu).
+constexpr int kRowSplit = 16;
+
 struct Workspace {
   // PatSearch per-tile statistics, [H][nb][128] each (log2 domain max, sums under it)
   float* st_m = nullptr;
@@ -33,6 +36,8 @@ struct Workspace {
   float* anc = nullptr;    // [H][2][128] anchor partial sums (tile 0, tile N_b-1)
   float* rowM = nullptr;   // [H][128]
   float* rowZ = nullptr;   // [H][128]
+  float2* row_part = nullptr;  // [H][kRowSplit][128] per-CTA (max, sum) partials of the row statistics
+  int* row_ticket = nullptr;   // [H] CTAs done per head (zero between launches)
   float* pv = nullptr;     // [H][nb] pooled vertical score
   float* pshi = nullptr;   // [H][nb] slash contribution of tile t to block N_b-1-t
   float* pslo = nullptr;   // [H][nb] slash contribution of tile t to block N_b-2-t
@@ -53,7 +58,7 @@ struct Workspace {
   int64_t* eq_off = nullptr;               // [H][nb+1]
   // per-row block masks and CSR
   uint32_t* rowmask = nullptr;  // [H][nb][nbw]
-  int64_t* row_cnt = nullptr;   // [H*nb]
+  int64_t* scan_blk = nullptr;  // [ceil(H*nb/1024)] per-1024-row totals, then offsets
   int64_t* row_ptr = nullptr;   // [H*nb+1]
   int32_t* col = nullptr;       // [col_cap]
   int64_t col_cap = 0;

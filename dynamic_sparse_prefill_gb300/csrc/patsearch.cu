@@ -267,37 +267,58 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
 }
 
 // Row maximum M_r and normaliser Z_r of every proxy row over all key tiles.
-__global__ void __launch_bounds__(1024) proxy_row_stats_kernel(const float* __restrict__ st_m,
-                                                               const float* __restrict__ st_u,
-                                                               const float* __restrict__ st_w,
-                                                               int nb, float* rowM,
-                                                               float* rowZ) {
-  __shared__ float sM[8][kBlk], sZ[8][kBlk];
-  const int h = blockIdx.x;
+__global__ void __launch_bounds__(256) proxy_row_stats_kernel(const float* __restrict__ st_m,
+                                                              const float* __restrict__ st_u,
+                                                              const float* __restrict__ st_w,
+                                                              int nb, float2* part, int* ticket,
+                                                              float* rowM, float* rowZ) {
+  // kRowSplit CTAs per head each merge a contiguous range of tiles into (max, sum) per row;
+  // the last CTA of the head to finish (ticket) merges the kRowSplit partials.
+  __shared__ float sM[2][kBlk], sZ[2][kBlk];
+  __shared__ int last;
+  const int h = blockIdx.y, sp = blockIdx.x;
   const int r = threadIdx.x & 127, slice = threadIdx.x >> 7;
+  const int per = (nb + kRowSplit - 1) / kRowSplit;
+  const int t0 = sp * per, t1 = min(nb, t0 + per);
   float M = -FLT_MAX, Z = 0.f;
-  for (int t = slice; t < nb; t += 8) {
+  for (int t = t0 + slice; t < t1; t += 2) {
     const size_t idx = (static_cast<size_t>(h) * nb + t) * kBlk + r;
     const float m = st_m[idx];
-    const float s = st_u[idx] + st_w[idx];
+    const float sum = st_u[idx] + st_w[idx];
     if (m > M) {
-      Z = Z * fast_exp2(M - m) + s;
+      Z = Z * fast_exp2(M - m) + sum;
       M = m;
     } else {
-      Z += s * fast_exp2(m - M);
+      Z += sum * fast_exp2(m - M);
     }
   }
   sM[slice][r] = M;
   sZ[slice][r] = Z;
   __syncthreads();
   if (slice == 0) {
+    const float Mt = fmaxf(sM[0][r], sM[1][r]);
+    const float Zt = sZ[0][r] * fast_exp2(sM[0][r] - Mt) + sZ[1][r] * fast_exp2(sM[1][r] - Mt);
+    part[(static_cast<size_t>(h) * kRowSplit + sp) * kBlk + r] = make_float2(Mt, Zt);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&ticket[h], 1) == kRowSplit - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (slice == 0) {
+    const float2* p = part + static_cast<size_t>(h) * kRowSplit * kBlk + r;
     float Mt = -FLT_MAX;
-    for (int i = 0; i < 8; ++i) Mt = fmaxf(Mt, sM[i][r]);
+    for (int i = 0; i < kRowSplit; ++i) Mt = fmaxf(Mt, __ldcg(&p[i * kBlk]).x);
     float Zt = 0.f;
-    for (int i = 0; i < 8; ++i) Zt += sZ[i][r] * fast_exp2(sM[i][r] - Mt);
+    for (int i = 0; i < kRowSplit; ++i) {
+      const float2 v = __ldcg(&p[i * kBlk]);
+      Zt += v.y * fast_exp2(v.x - Mt);
+    }
     rowM[h * kBlk + r] = Mt;
     rowZ[h * kBlk + r] = Zt;
   }
+  if (threadIdx.x == 0) ticket[h] = 0;
 }
 
 // Pooled vertical and slash contributions of every key tile: a warp per tile.
@@ -639,7 +660,9 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   proxy_tile_stats_kernel<<<dim3(s.H, nchunks), kProxyThreads, kProxySmem, st>>>(tmQ, tmK, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  proxy_row_stats_kernel<<<s.H, 1024, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb, w.rowM, w.rowZ);
+  proxy_row_stats_kernel<<<dim3(kRowSplit, s.H), 256, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb,
+                                                               w.row_part, w.row_ticket, w.rowM,
+                                                               w.rowZ);
   proxy_pool_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(
       w.st_m, w.st_u, w.st_w, w.rowM, w.rowZ, s.nb, 1.f / kBlk, w.pv, w.pshi, w.pslo);
   RouteArgs r;
@@ -694,7 +717,7 @@ cudaError_t init_patsearch_attributes() {
 // below, which lives in every GPU's memory from the time the library is loaded until
 // the process exits.  It holds at most kStaticMaxHeads query heads and
 // kStaticMaxTiles (query head, key tile) pairs, i.e. batch*hq*(n/128) <= 8192: for
-// example 32 heads at 32k tokens or 8 heads at 128k tokens.  About 13 MB.
+// example 32 heads at 32k tokens or 8 heads at 128k tokens.  About 15 MB.
 // ---------------------------------------------------------------------------------------
 #include <mutex>
 
@@ -719,7 +742,9 @@ constexpr size_t kOffMu = kOffPs + align256(sizeof(float) * kStaticMaxTiles);
 constexpr size_t kOffCounts = kOffMu + align256(sizeof(float) * kStaticMaxHeads * 2);
 constexpr size_t kOffSelv = kOffCounts + align256(sizeof(int32_t) * kStaticMaxHeads * 4);
 constexpr size_t kOffSels = kOffSelv + align256(kStaticMaxTiles);
-constexpr size_t kOffErr = kOffSels + align256(kStaticMaxTiles);
+constexpr size_t kOffPart = kOffSels + align256(kStaticMaxTiles);
+constexpr size_t kOffTicket = kOffPart + align256(sizeof(float2) * kStaticMaxHeads * kRowSplit * kBlk);
+constexpr size_t kOffErr = kOffTicket + align256(sizeof(int) * kStaticMaxHeads);
 constexpr size_t kStaticBytes = kOffErr + 256;
 
 // The scratch of crisp_route_static.  In host code this name is only a stand-in: the
@@ -835,6 +860,8 @@ extern "C" crisp_status crisp_route_static(const crisp_dims* dims, const void* Q
   w.counts = reinterpret_cast<int32_t*>(b + kOffCounts);
   w.selv = b + kOffSelv;
   w.sels = b + kOffSels;
+  w.row_part = reinterpret_cast<float2*>(b + kOffPart);
+  w.row_ticket = reinterpret_cast<int*>(b + kOffTicket);
   w.err = reinterpret_cast<uint32_t*>(b + kOffErr);
   w.cstruct = c_struct;
   w.route = route_vs;
@@ -844,9 +871,12 @@ extern "C" crisp_status crisp_route_static(const crisp_dims* dims, const void* Q
       !static_map(su->encode, &tmK, K, static_cast<int64_t>(s.Hkv) * s.n))
     return CRISP_ERR_CUDA;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  // The error word is the only scratch that must start at zero; every other scratch
-  // value is written before it is read.
-  if (cudaMemsetAsync(w.err, 0, sizeof(uint32_t), cs) != cudaSuccess) return CRISP_ERR_CUDA;
+  // The error word and the row-statistics tickets are the only scratch that must start at
+  // zero (the tickets also return to zero after every use); every other scratch value is
+  // written before it is read.
+  if (cudaMemsetAsync(w.err, 0, sizeof(uint32_t), cs) != cudaSuccess ||
+      cudaMemsetAsync(w.row_ticket, 0, sizeof(int) * s.H, cs) != cudaSuccess)
+    return CRISP_ERR_CUDA;
   if (launch_patsearch(&c, s, *cfg, tmQ, tmK, cs) != cudaSuccess) return CRISP_ERR_CUDA;
   if (cudaMemcpyAsync(status, w.err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, cs) !=
       cudaSuccess)

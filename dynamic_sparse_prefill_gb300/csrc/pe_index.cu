@@ -83,8 +83,11 @@ __global__ void __launch_bounds__(128) pe_pool_k_kernel(const uint16_t* __restri
 }
 
 // ---------------------------------------------------------------- pooled logits
-// logits[I][K] = Qbar_I . Kbar_K / sqrt(d) for K <= I, in 64 x 64 tiles (fp32 FMA).
-constexpr int kPT = 64;
+// logits[I][K] = Qbar_I . Kbar_K / sqrt(d) for K <= I, in 128 x 128 tiles (fp32 FMA).  Each
+// thread accumulates 8 x 8 outputs (rows ty + 16i, columns tx + 16j), so a step over d
+// takes 16 shared-memory loads for 64 FMAs, and the loads of a warp fall in distinct banks
+// (the tiles are stored transposed, [d][row], with a row pitch of 129 floats).
+constexpr int kPT = 128;
 __global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict__ qbar,
                                                         const float* __restrict__ kbar,
                                                         const uint8_t* __restrict__ route,
@@ -96,7 +99,11 @@ __global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict_
   const int hk = (h / hq) * hkv + (h % hq) / group;
   __shared__ float sq[32][kPT + 1], sk[32][kPT + 1];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
   for (int d0 = 0; d0 < kD; d0 += 32) {
     for (int i = threadIdx.x; i < kPT * 32; i += 256) {
       const int row = i >> 5, dd = i & 31;
@@ -105,26 +112,26 @@ __global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict_
       sk[dd][row] = K < nb ? kbar[(static_cast<size_t>(hk) * nb + K) * kD + d0 + dd] : 0.f;
     }
     __syncthreads();
-#pragma unroll 8
+#pragma unroll 4
     for (int dd = 0; dd < 32; ++dd) {
-      float a[4], b[4];
+      float a[8], b[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = sq[dd][ty * 4 + i];
-        b[i] = sk[dd][tx * 4 + i];
+      for (int i = 0; i < 8; ++i) {
+        a[i] = sq[dd][ty + 16 * i];
+        b[i] = sk[dd][tx + 16 * i];
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int I = I0 + ty * 4 + i, K = K0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int I = I0 + ty + 16 * i, K = K0 + tx + 16 * j;
       if (I < nb && K <= I) pev[(static_cast<size_t>(h) * nb + I) * nb + K] = acc[i][j] * scale;
     }
 }
@@ -190,12 +197,18 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
   if (route[h]) return;
   const PeState st = pe[h];
   if (st.select_all) return;
-  // Per-CTA histogram with native fp32 shared-memory atomics; the CTA's partial masses
-  // (each at most a few percent of the total) are combined in fp64 in global memory.
-  __shared__ unsigned int scnt[256];
-  __shared__ float smass[256];
-  scnt[threadIdx.x] = 0;
-  smass[threadIdx.x] = 0.f;
+  // Per-warp histograms with native fp32 shared-memory atomics (later passes see many
+  // values in few bins, so one shared copy serialises the warps); the CTA's partial
+  // masses (each at most a few percent of the total) are combined in fp64 in global
+  // memory.
+  __shared__ unsigned int scnt[8][256];
+  __shared__ float smass[8][256];
+  const int wp = threadIdx.x >> 5;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    scnt[w][threadIdx.x] = 0;
+    smass[w][threadIdx.x] = 0.f;
+  }
   __syncthreads();
   // Each thread keeps a run (bin, count, fp32 mass) and flushes it to the shared
   // histogram only when the bin changes: the early passes see long runs of one bin.
@@ -207,8 +220,8 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
     const uint32_t bin = (bits >> shift) & 255u;
     if (bin != cur) {
       if (cnt) {
-        atomicAdd(&scnt[cur], cnt);
-        atomicAdd(&smass[cur], mass);
+        atomicAdd(&scnt[wp][cur], cnt);
+        atomicAdd(&smass[wp][cur], mass);
       }
       cur = bin;
       cnt = 0;
@@ -242,13 +255,20 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
     }
   }
   if (cnt) {
-    atomicAdd(&scnt[cur], cnt);
-    atomicAdd(&smass[cur], mass);
+    atomicAdd(&scnt[wp][cur], cnt);
+    atomicAdd(&smass[wp][cur], mass);
   }
   __syncthreads();
-  if (scnt[threadIdx.x]) {
-    atomicAdd(&hist_cnt[h * 256 + threadIdx.x], static_cast<unsigned long long>(scnt[threadIdx.x]));
-    atomicAdd(&hist_mass[h * 256 + threadIdx.x], static_cast<double>(smass[threadIdx.x]));
+  unsigned int c = 0;
+  double m = 0.0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    c += scnt[w][threadIdx.x];
+    m += static_cast<double>(smass[w][threadIdx.x]);
+  }
+  if (c) {
+    atomicAdd(&hist_cnt[h * 256 + threadIdx.x], static_cast<unsigned long long>(c));
+    atomicAdd(&hist_mass[h * 256 + threadIdx.x], m);
   }
 }
 
@@ -315,9 +335,10 @@ __global__ void __launch_bounds__(256) pe_eqcount_kernel(const float* __restrict
   const int h = blockIdx.y, I = blockIdx.x;
   if (route[h]) return;
   const PeState st = pe[h];
+  if (st.select_all || st.need_eq >= st.count_eq) return;  // no tie ranks needed
   __shared__ int red[8];
   int c = 0;
-  if (!st.select_all) {
+  {
     const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
     for (int K = threadIdx.x; K <= I; K += 256) c += __float_as_uint(row[K]) == st.thresh;
   }
@@ -334,9 +355,12 @@ __global__ void __launch_bounds__(256) pe_eqcount_kernel(const float* __restrict
 
 // In-place exclusive scan of the per-row counts of one head (nb <= 8192 entries).
 __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restrict__ route,
-                                                         int nb, int64_t* eq_off) {
+                                                         const PeState* __restrict__ pe, int nb,
+                                                         int64_t* eq_off) {
   const int h = blockIdx.x;
   if (route[h]) return;
+  const PeState st = pe[h];
+  if (st.select_all || st.need_eq >= st.count_eq) return;  // no tie ranks needed
   __shared__ int64_t part[1024];
   int64_t* a = eq_off + static_cast<size_t>(h) * (nb + 1);
   const int per = (nb + 1023) / 1024;
@@ -360,53 +384,60 @@ __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restri
   if (threadIdx.x == 1023) a[nb] = part[1023];
 }
 
-// Row masks of PE heads: v > T, or v == T with flat rank < need; plus the diagonal.
+// Row masks of PE heads: v > T, or v == T with flat rank < need; plus the diagonal.  A warp
+// per row, four 32-key words in flight per lane.  Flat-order tie ranks are needed only
+// when some but not all items equal to the threshold are taken (need_eq < count_eq).
 __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ pev,
                                                       const uint8_t* __restrict__ route,
                                                       const PeState* __restrict__ pe,
                                                       const int64_t* __restrict__ eq_off,
                                                       int nb, int nbw, uint32_t* rowmask,
                                                       int32_t* counts) {
-  const int h = blockIdx.y, I = blockIdx.x;
+  const int h = blockIdx.y;
   if (route[h]) return;
-  const PeState st = pe[h];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ int weq[8];
-  __shared__ int wsel[8];
+  const int I = blockIdx.x * 8 + warp;
+  if (I >= nb) return;
+  const PeState st = pe[h];
+  const bool all = st.select_all != 0;
+  const bool rank_ties = !all && st.need_eq < st.count_eq;
+  int64_t eq_base = rank_ties ? eq_off[static_cast<size_t>(h) * (nb + 1) + I] : 0;
   const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
   uint32_t* mrow = rowmask + (static_cast<size_t>(h) * nb + I) * nbw;
-  int64_t eq_base = st.select_all ? 0 : eq_off[static_cast<size_t>(h) * (nb + 1) + I];
+  const int nw = (I >> 5) + 1;  // words holding keys K <= I
   int selected = 0;
-  for (int K0 = 0; K0 < nbw * 32; K0 += 256) {
-    const int K = K0 + threadIdx.x;
-    const bool valid = K <= I;
-    const uint32_t bits = valid ? __float_as_uint(row[K]) : 0u;
-    const bool eq = valid && !st.select_all && bits == st.thresh;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) weq[warp] = __popc(beq);
-    __syncthreads();
-    int wpre = 0, tot = 0;
-    for (int i = 0; i < 8; ++i) {
-      if (i < warp) wpre += weq[i];
-      tot += weq[i];
+  for (int wd0 = 0; wd0 < nw; wd0 += 4) {
+    uint32_t x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int K = (wd0 + u) * 32 + lane;
+      x[u] = K <= I ? __float_as_uint(row[K]) : 0u;
     }
-    const int64_t rank = eq_base + wpre + __popc(beq & ((1u << lane) - 1u));
-    bool sel = valid && (st.select_all || bits > st.thresh ||
-                         (eq && rank < static_cast<int64_t>(st.need_eq)));
-    const unsigned word = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) {
-      wsel[warp] = __popc(word);
-      const int wd = (K0 >> 5) + warp;
-      uint32_t out = word;
-      if (I >= wd * 32 && I < wd * 32 + 32) out |= 1u << (I & 31);
-      if (wd < nbw) mrow[wd] = out;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int wd = wd0 + u;
+      if (wd >= nw) break;
+      const bool valid = wd * 32 + lane <= I;
+      bool sel = valid && (all || x[u] > st.thresh);
+      if (!all) {
+        const bool eq = valid && x[u] == st.thresh;
+        if (rank_ties) {
+          const unsigned beq = __ballot_sync(0xffffffffu, eq);
+          const int64_t rank = eq_base + __popc(beq & ((1u << lane) - 1u));
+          sel = sel || (eq && rank < static_cast<int64_t>(st.need_eq));
+          eq_base += __popc(beq);
+        } else {
+          sel = sel || eq;
+        }
+      }
+      unsigned word = __ballot_sync(0xffffffffu, sel);
+      selected += __popc(word);
+      if (wd == (I >> 5)) word |= 1u << (I & 31);
+      if (lane == 0) mrow[wd] = word;
     }
-    __syncthreads();
-    for (int i = 0; i < 8; ++i) selected += wsel[i];
-    eq_base += tot;
-    __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  for (int wd = nw + lane; wd < nbw; wd += 32) mrow[wd] = 0u;
+  if (lane == 0) {
     atomicAdd(&counts[h * 4 + 0], selected);
     if (selected == 0) atomicAdd(&counts[h * 4 + 1], 1);
   }
@@ -435,9 +466,9 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
                                          w.hist_mass);
   }
   pe_eqcount_kernel<<<dim3(s.nb, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, s.nb, w.eq_off);
-  pe_eqscan_kernel<<<s.H, 1024, 0, st>>>(w.route, s.nb, w.eq_off);
-  pe_mask_kernel<<<dim3(s.nb, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, w.eq_off, s.nb, s.nbw,
-                                                  w.rowmask, w.counts);
+  pe_eqscan_kernel<<<s.H, 1024, 0, st>>>(w.route, w.pe, s.nb, w.eq_off);
+  pe_mask_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, w.eq_off, s.nb,
+                                                            s.nbw, w.rowmask, w.counts);
   return cudaGetLastError();
 }
 

@@ -225,7 +225,7 @@ const char* crisp_status_string(crisp_status s);
  * with H = batch*hq.  Only enqueues work on `stream`; read the outputs after
  * synchronising it.
  *
- * Scratch is a fixed array in the library's device memory (about 13 MB on every GPU
+ * Scratch is a fixed array in the library's device memory (about 15 MB on every GPU
  * that loads the library, held until the process exits).  Limits: batch*hq <= 128 and
  * batch*hq*(n/128) <= 8192; larger problems return CRISP_ERR_UNSUPPORTED before any work
  * is queued.  Other shape and parameter rules are those of crisp_select.  The first call
