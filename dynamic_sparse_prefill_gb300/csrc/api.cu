@@ -272,6 +272,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.len_hist), sizeof(int32_t) * (Hkv * (nb + 1) + 2)},
       {reinterpret_cast<void**>(&w.redo), sizeof(int32_t) * H * nb},
       {reinterpret_cast<void**>(&w.redo_count), sizeof(int)},
+      {reinterpret_cast<void**>(&w.work_ctr), sizeof(int) * Hkv},
       {reinterpret_cast<void**>(&w.err), sizeof(uint32_t)},
   };
   size_t total = 0;

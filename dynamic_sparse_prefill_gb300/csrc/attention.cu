@@ -166,6 +166,8 @@ struct AttnArgs {
   // maximum are appended here for the rescue pass.
   int32_t* redo;
   int* redo_count;
+  // Fast pass: the launch's work counter (items are handed out in order, see ring_take).
+  int* work_ctr;
 };
 
 struct Item {
@@ -173,17 +175,10 @@ struct Item {
   int64_t beg;
 };
 
-// Work item k of a CTA's round-robin sequence (k = blockIdx.x + i * G).  Items are taken
-// in waves of G consecutive entries of the order; odd waves are walked in reverse
-// (serpentine), so each CTA's total work stays balanced and the CTAs of a wave start and
-// advance together over the same key blocks -- the order keeps one KV head's rows
-// together, so those blocks are fetched from DRAM once per wave and served from L2.
-// Dense order: KV head major, then query block descending, then the group's q-heads.
-__device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G, int num_items) {
-  const int m = k / G, pos = k % G;
-  const int base = m * G;
-  const int wsize = min(G, num_items - base);
-  const int ke = ((m & 1) ? base + wsize - 1 - pos : k) + a.item_base;
+// Item at position ke of the launch's order: a listed row (rescue pass), a row of the
+// sparse order, or the dense enumeration (KV head major, query block descending, the
+// group's q-heads adjacent).
+__device__ __forceinline__ Item item_of(const AttnArgs& a, int ke) {
   Item it;
   if (a.list != nullptr) {
     const int row = a.list[ke];
@@ -209,6 +204,17 @@ __device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G, int nu
     it.L = static_cast<int>(a.row_ptr[row + 1] - it.beg);
   }
   return it;
+}
+
+// Work item k of a CTA's static round-robin sequence (k = blockIdx.x + i * G): items are
+// taken in waves of G consecutive entries of the order, odd waves in reverse
+// (serpentine), so each CTA's total stays balanced.  Used by the rescue pass.
+__device__ __forceinline__ Item get_item(const AttnArgs& a, int k, int G, int num_items) {
+  const int m = k / G, pos = k % G;
+  const int base = m * G;
+  const int wsize = min(G, num_items - base);
+  const int ke = ((m & 1) ? base + wsize - 1 - pos : k) + a.item_base;
+  return item_of(a, ke);
 }
 
 __device__ __forceinline__ int block_of(const AttnArgs& a, const Item& it, int j) {
@@ -289,6 +295,122 @@ __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, cons
       const int row = it.hk * a.n + kb * kBlk;
       mbar_arrive_expect_tx(&v_full[s], kTileBytes);
       tma_load_3d(dst, tmV, &v_full[s], 0, row, 0);
+      ++gv;
+    }
+  }
+  for (int g = max(0, gv - kVS); g < gv; ++g)
+    drain_wait(&v_full[g % kVS], (g / kVS) & 1, a.err, tmo);
+}
+
+// ---------------------------------------------------------------------------------------
+// Dynamic item feed of the fast pass.  The Q/K producer takes the next position of the
+// launch's order from a global counter when it starts an item (so CTAs that finish early
+// take more items: longest-first greedy balancing, since the order is longest first) and
+// publishes it in a kItemRing-slot ring in shared memory; every other role reads the
+// ring in order and releases the slot.  -1 ends the stream.
+constexpr int kItemRing = 4;
+constexpr int kItemReaders = 11;  // V producer, S issuer, P.V issuer, 8 softmax warps
+
+struct ItemFeed {
+  volatile int* slot;
+  uint64_t* full;   // [kItemRing] count 1
+  uint64_t* empty;  // [kItemRing] count kItemReaders
+};
+
+// One thread: the idx-th item of the stream (-1: end), or -2 if a wait ran out.
+__device__ __forceinline__ int feed_next(const ItemFeed& f, int idx, uint32_t* err,
+                                         volatile int* abort_flag, uint64_t tmo) {
+  const int s = idx % kItemRing;
+  if (!mbar_wait(&f.full[s], (idx / kItemRing) & 1, err, abort_flag, tmo)) return -2;
+  const int k = f.slot[s];
+  mbar_arrive(&f.empty[s]);
+  return k;
+}
+
+// A whole warp: the same, one release per warp.
+__device__ __forceinline__ int feed_next_warp(const ItemFeed& f, int idx, uint32_t* err,
+                                              volatile int* abort_flag, uint64_t tmo) {
+  const int s = idx % kItemRing;
+  if (!warp_wait(&f.full[s], (idx / kItemRing) & 1, err, abort_flag, tmo)) return -2;
+  const int k = f.slot[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&f.empty[s]);
+  return k;
+}
+
+// The fast pass's Q/K producer: takes items from the counter, publishes them, and loads
+// Q and the K blocks exactly as produce_qk does for its static sequence.
+template <int kKS>
+__device__ __forceinline__ void produce_qk_feed(const AttnArgs& a, int num_items,
+                                                const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                                uint8_t* sQ, uint8_t* sK, uint64_t* q_full,
+                                                uint64_t* q_empty, uint64_t* k_full,
+                                                uint64_t* k_empty, const ItemFeed& feed,
+                                                volatile int* abort_flag, uint64_t tmo) {
+  tma_prefetch_desc(tmQ);
+  tma_prefetch_desc(tmK);
+  int gk = 0, q_loads = 0;
+  bool ok = true;
+  for (int item_idx = 0; ok; ++item_idx) {
+    const int s = item_idx % kItemRing;
+    if (item_idx >= kItemRing &&
+        !mbar_wait(&feed.empty[s], ((item_idx / kItemRing) - 1) & 1, a.err, abort_flag, tmo))
+      break;
+    int k = atomicAdd(a.work_ctr, 1);
+    if (k >= num_items) k = -1;
+    feed.slot[s] = k;
+    mbar_arrive(&feed.full[s]);
+    if (k < 0) break;
+    const Item it = item_of(a, a.item_base + k);
+    if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) break;
+    const int qrow = it.h * a.n + it.I * kBlk;
+    mbar_arrive_expect_tx(q_full, kTileBytes);
+    tma_load_3d(sQ, tmQ, q_full, 0, qrow, 0);
+    ++q_loads;
+    for (int j = 0; j < it.L; ++j) {
+      int kb = block_of(a, it, j);
+      if (kb < 0 || kb > it.I) {
+        atomicOr(a.err, kErrRange);
+        kb = it.I;
+      }
+      const int ks = gk % kKS;
+      if (gk >= kKS && !mbar_wait(&k_empty[ks], ((gk / kKS) + 1) & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&k_full[ks], kTileBytes);
+      tma_load_3d(sK + ks * kTileBytes, tmK, &k_full[ks], 0, it.hk * a.n + kb * kBlk, 0);
+      ++gk;
+    }
+  }
+  if (q_loads > 0) drain_wait(q_full, (q_loads - 1) & 1, a.err, tmo);
+  for (int g = max(0, gk - kKS); g < gk; ++g)
+    drain_wait(&k_full[g % kKS], (g / kKS) & 1, a.err, tmo);
+}
+
+// The fast pass's V producer: the items of the feed, in order.
+template <int kVS>
+__device__ __forceinline__ void produce_v_feed(const AttnArgs& a, const CUtensorMap* tmV,
+                                               uint8_t* sV, uint64_t* v_full, uint64_t* v_empty,
+                                               const ItemFeed& feed, volatile int* abort_flag,
+                                               uint64_t tmo) {
+  tma_prefetch_desc(tmV);
+  int gv = 0;
+  bool ok = true;
+  for (int item_idx = 0; ok; ++item_idx) {
+    const int k = feed_next(feed, item_idx, a.err, abort_flag, tmo);
+    if (k < 0) break;
+    const Item it = item_of(a, a.item_base + k);
+    for (int j = 0; j < it.L; ++j) {
+      int kb = block_of(a, it, j);
+      if (kb < 0 || kb > it.I) kb = it.I;
+      const int s = gv % kVS;
+      if (gv >= kVS && !mbar_wait(&v_empty[s], ((gv / kVS) + 1) & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&v_full[s], kTileBytes);
+      tma_load_3d(sV + s * kTileBytes, tmV, &v_full[s], 0, it.hk * a.n + kb * kBlk, 0);
       ++gv;
     }
   }
@@ -595,7 +717,7 @@ constexpr int kFastVStages = 2;
 // block is always g - 2 and the V slot of block g is P_t's slot too: one commit after P.V
 // (v_empty[g & 1]) frees both the V slot and the P buffer.
 static_assert(kFastVStages == 2, "v_empty doubles as the P buffers' release");
-constexpr size_t kSmemFast = kTileBytes * (1 + kFastKStages + kFastVStages) + kXBytes + 256;
+constexpr size_t kSmemFast = kTileBytes * (1 + kFastKStages + kFastVStages) + kXBytes + 512;
 
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -627,8 +749,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* x_ready = o_free + 1;                // both tiles' first-block maxima are in sXM
   uint64_t* l_ready = x_ready + 1;               // both tiles' row sums are in sXL
   uint64_t* drain = l_ready + 1;                 // [2] one per MMA-issuing thread
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* feed_full = drain + 2;               // [kItemRing]
+  uint64_t* feed_empty = feed_full + kItemRing;  // [kItemRing]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(feed_empty + kItemRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const ItemFeed feed{reinterpret_cast<volatile int*>(tmem_slot + 2), feed_full, feed_empty};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns;
@@ -656,6 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(l_ready, 8);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&feed_full[i], 1);
+      mbar_init(&feed_empty[i], kItemReaders);
+    }
     *sRedo = 0;
     *abort_flag = 0;
     fence_barrier_init();
@@ -672,11 +801,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kLoaderRegs>();
     if (warp == 8) {
       if (lane == 0)
-        produce_qk<kFastKStages>(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full,
-                                 k_empty, abort_flag, tmo);
+        produce_qk_feed<kFastKStages>(a, num_items, &tmQ, &tmK, sQ, sK, q_full, q_empty, k_full,
+                                      k_empty, feed, abort_flag, tmo);
     } else if (warp == 10) {
       if (lane == 0)
-        produce_v<kFastVStages>(a, num_items, &tmV, sV, v_full, v_empty, abort_flag, tmo);
+        produce_v_feed<kFastVStages>(a, &tmV, sV, v_full, v_empty, feed, abort_flag, tmo);
     } else if (warp == 9) {
       // ---------------------------------------------------------------- S issuer
       // S_j = Q K_j^T into tile (j & 1)'s buffer, as soon as the tile's softmax has loaded
@@ -689,8 +818,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // barrier phases follow from g alone (phase of block g: (g >> 1) & 1).
         int gk = 0, item_idx = 0;
         bool ok = true;
-        for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
-          const Item it = get_item(a, k, gridDim.x, num_items);
+        for (; ok; ++item_idx) {
+          const int kf = feed_next(feed, item_idx, a.err, abort_flag, tmo);
+          if (kf < 0) break;
+          const Item it = item_of(a, a.item_base + kf);
           if (!mbar_wait(q_full, item_idx & 1, a.err, abort_flag, tmo)) {
             ok = false;
             break;
@@ -728,8 +859,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dV0 = sdesc_sw128(smem_u32(sV), kTileBytes / 2, 1024);
         int gv = 0, item_idx = 0;
         bool ok = true;
-        for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
-          const Item it = get_item(a, k, gridDim.x, num_items);
+        for (; ok; ++item_idx) {
+          const int kf = feed_next(feed, item_idx, a.err, abort_flag, tmo);
+          if (kf < 0) break;
+          const Item it = item_of(a, a.item_base + kf);
           for (int j = 0; j < it.L; ++j) {
             const int t = gv & 1;
             const int s = gv % kFastVStages;  // == t
@@ -782,8 +915,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&s_free[t]);
       return true;
     };
-    for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x, ++item_idx) {
-      const Item it = get_item(a, k, gridDim.x, num_items);
+    for (; ok; ++item_idx) {
+      const int kf = feed_next_warp(feed, item_idx, a.err, abort_flag, tmo);
+      if (kf < 0) break;
+      const Item it = item_of(a, a.item_base + kf);
       const int j0 = (t ^ gbase) & 1;  // this tile's first block: (gbase + j0) & 1 == t
       // Row reference: the larger of the two tiles' first-block row maxima.
       float mfirst = -FLT_MAX;
@@ -976,10 +1111,14 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   // head).  A group holds enough rows for 8 per SM.
   const int per_kv = s.group * s.nb;
   const int per = attention_kv_heads_per_launch(s, ctx->num_sms);
+  const int nlaunch = (s.Hkv + per - 1) / per;
+  e = cudaMemsetAsync(ctx->ws.work_ctr, 0, sizeof(int) * nlaunch, st);
+  if (e != cudaSuccess) return e;
   for (int g0 = 0; g0 < s.Hkv; g0 += per) {
     const int m = min(per, s.Hkv - g0);
     a.item_base = g0 * per_kv;
     a.num_items = m * per_kv;
+    a.work_ctr = ctx->ws.work_ctr + g0 / per;
     const int grid = a.num_items < ctx->num_sms ? a.num_items : ctx->num_sms;
     attention_kernel<<<grid, kThreads, kSmemFast, st>>>(tmQ, tmK, tmV, a);
   }
@@ -991,6 +1130,7 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   r.list_count = ctx->ws.redo_count;
   r.redo = nullptr;
   r.redo_count = nullptr;
+  r.work_ctr = nullptr;
   attention_rescue_kernel<<<ctx->num_sms, kThreads, kSmem, st>>>(tmQ, tmK, tmV, r);
   return cudaGetLastError();
 }

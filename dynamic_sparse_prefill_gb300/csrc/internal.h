@@ -68,6 +68,7 @@ struct Workspace {
   // rows the fast attention pass hands to the rescue pass (see attention.cu)
   int32_t* redo = nullptr;      // [H*nb]
   int* redo_count = nullptr;
+  int* work_ctr = nullptr;      // [Hkv] per-launch item counters of the fast attention pass
   uint32_t* err = nullptr;      // device error word
 };
 
