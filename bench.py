@@ -50,23 +50,35 @@ def algorithmic_flops(nnz: int, rows: int) -> float:
     return 4.0 * B * B * D * (nnz - rows) + 2.0 * D * B * (B + 1) * rows
 
 
+def kernel_code_hash(path: str) -> str:
+    """sha256 of a CUDA source with // comments and blank lines removed: the counters of a
+    capture stay valid while only the comments change."""
+    import hashlib
+    import re
+    lines = []
+    for line in open(path).read().splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line.strip():
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes of one crisp_attend (summed over its attention-kernel launches) from the
-    committed ncu summary, if it was taken on this workload with the current kernel
-    source; else None."""
-    import hashlib
+    committed ncu summary, if it was taken on this workload with the current kernel code;
+    else None."""
     import re
     prof = os.path.join(ROOT, "profiles", f"attention_kernel_{workload}_traffic.md")
     src = os.path.join(ROOT, "dynamic_sparse_prefill_gb300", "csrc", "attention.cu")
     if not os.path.exists(prof):
         return None
     text = open(prof).read()
-    m = re.search(r"source_sha256: ([0-9a-f]{64})", text)
+    m = re.search(r"code_sha256: ([0-9a-f]{64})", text)
     rd = re.search(r"dram_bytes_read: (\d+)", text)
     wr = re.search(r"dram_bytes_write: (\d+)", text)
     if not (m and rd and wr):
         return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m.group(1):
+    if kernel_code_hash(src) != m.group(1):
         return None
     return int(rd.group(1)) + int(wr.group(1))
 

@@ -7,15 +7,20 @@
 // "Method step details" step 4 applies it to the selected index set.  With every key
 // block K <= I selected this is dense causal attention, the speedup denominator.
 //
-// Two persistent kernels, one CTA per SM, walking work items (query head h, query block
-// I) in serpentine waves over an order that keeps each KV head's rows together, longest
-// first (see get_item).  Both use the same warp roles:
-//   warps 0-3  softmax of "tile 0": the even-numbered key blocks of the item's list;
-//   warps 4-7  softmax of "tile 1": the odd-numbered key blocks;
-//   warp 8     TMA producer of the item's Q tile and K_j (3-slot ring);
-//   warp 9     MMA issuer (one thread, tcgen05): S = Q K_j^T into TMEM, then O += P V_j
-//              with P read from TMEM;
-//   warp 10    TMA producer of V_j (2-slot ring), so K prefetch never waits on a V slot.
+// Two persistent kernels, one CTA per SM, over work items (query head h, query block I)
+// in an order that keeps each KV head's rows together, longest first.  The fast kernel
+// hands items out dynamically (a per-launch counter and a shared-memory item ring, see
+// ItemFeed); the rescue kernel walks its short list in static serpentine waves (see
+// get_item).  Both use the same warp roles:
+//   warps 0-3  softmax of "tile 0" and warps 4-7 of "tile 1": the tiles take alternate
+//              key blocks (by the CTA-wide block index in the fast kernel, by the index
+//              within the row in the rescue kernel);
+//   warp 8     TMA producer of the item's Q tile and K_j (4-slot ring in the fast
+//              kernel, 3-slot in the rescue kernel);
+//   warp 9     MMA issuer (one thread, tcgen05): S = Q K_j^T into TMEM (and, in the
+//              rescue kernel, O += P V_j with P read from TMEM);
+//   warp 10    TMA producer of V_j (2-slot ring), so K prefetch never waits on a V slot;
+//   warp 11    (fast kernel) the second MMA issuer: O += P V_j.
 // The softmax warpgroups take registers from the loader warpgroup (setmaxnreg).
 //
 // attention_kernel (every item): each tile has its own S and P buffers in TMEM and the
