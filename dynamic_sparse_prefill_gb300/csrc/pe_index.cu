@@ -210,25 +210,33 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
     smass[w][threadIdx.x] = 0.f;
   }
   __syncthreads();
-  // Each thread keeps a run (bin, count, fp32 mass) and flushes it to the shared
-  // histogram only when the bin changes: the early passes see long runs of one bin.
-  uint32_t cur = 0xFFFFFFFFu, cnt = 0;
-  float mass = 0.f;
+  // Each thread caches two (bin, count, fp32 mass) entries and flushes one to the shared
+  // histogram only when a third bin appears: the early passes see long runs of one bin,
+  // the later ones values alternating between neighbouring bins.
+  uint32_t b0 = 0xFFFFFFFFu, b1 = 0xFFFFFFFFu, c0 = 0, c1 = 0;
+  float m0 = 0.f, m1 = 0.f;
   auto take = [&](float v) {
     const uint32_t bits = __float_as_uint(v);
     if ((bits & st.decided) != st.prefix) return;
     const uint32_t bin = (bits >> shift) & 255u;
-    if (bin != cur) {
-      if (cnt) {
-        atomicAdd(&scnt[wp][cur], cnt);
-        atomicAdd(&smass[wp][cur], mass);
+    if (bin == b0) {
+      ++c0;
+      m0 += v;
+    } else if (bin == b1) {
+      ++c1;
+      m1 += v;
+    } else {
+      if (c1) {
+        atomicAdd(&scnt[wp][b1], c1);
+        atomicAdd(&smass[wp][b1], m1);
       }
-      cur = bin;
-      cnt = 0;
-      mass = 0.f;
+      b1 = b0;
+      c1 = c0;
+      m1 = m0;
+      b0 = bin;
+      c0 = 1;
+      m0 = v;
     }
-    ++cnt;
-    mass += v;
   };
   const int I0 = blockIdx.x * kHistRows;
   for (int I = I0; I < min(nb, I0 + kHistRows); ++I) {
@@ -254,9 +262,13 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
       for (int K = threadIdx.x; K < len; K += 256) take(row[K]);
     }
   }
-  if (cnt) {
-    atomicAdd(&scnt[wp][cur], cnt);
-    atomicAdd(&smass[wp][cur], mass);
+  if (c0) {
+    atomicAdd(&scnt[wp][b0], c0);
+    atomicAdd(&smass[wp][b0], m0);
+  }
+  if (c1) {
+    atomicAdd(&scnt[wp][b1], c1);
+    atomicAdd(&smass[wp][b1], m1);
   }
   __syncthreads();
   unsigned int c = 0;

@@ -260,6 +260,32 @@ def test_prefill_host_matches_device_path(dsp, name):
     ctx.close()
 
 
+def test_prefill_host_batch_two_uneven_chunks(dsp):
+    """crisp_prefill_host with batch 2 and 4 KV heads per entry (8 flattened KV heads) at
+    32k: the chunks hold 3, 3 and 2 KV heads, so the second spans both batch entries in the
+    flattened layout and the last is smaller; the output must match the device path."""
+    n, hq, hkv = 32768, 8, 4
+    g = random_qkv(n, 2 * hq, 2 * hkv, 128, seed=57, scale=3.0)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(2, n, hq, hkv)
+    ctx = dsp.Context(dims)
+    cfg = dsp.default_cfg()
+    o = torch.empty_like(q)
+    ctx.prefill(dims, q, k, v, cfg, o)
+    assert ctx.sync_status() == 0
+    ref = o.float().cpu().numpy().astype(np.float64)
+    t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = t(g["q"]), t(g["k"]), t(g["v"])
+    oh = torch.zeros(o.shape, dtype=torch.bfloat16).pin_memory()
+    q2, k2, v2, o2 = (torch.empty_like(x) for x in (q, k, v, o))
+    ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q2, k2, v2, o2)
+    assert ctx.sync_status() == 0
+    got = oh.float().numpy()
+    for h in range(2 * hq):
+        compare_outputs(got[h], ref[h], f"prefill_host batch 2, head {h}")
+    ctx.close()
+
+
 def test_timeout_is_reported_and_context_recovers(dsp):
     """A dropped barrier arrive makes a bounded wait run out: the kernel exits, the host
     reads CRISP_ERR_TIMEOUT, and the next call on the same context succeeds."""
