@@ -389,7 +389,26 @@ crisp_status crisp_prefill_host(crisp_ctx ctx, const crisp_dims* dims, const voi
   int per = (8 * ctx->num_sms + rows_per_kv - 1) / rows_per_kv;
   per = std::max(per, (s.Hkv + crisp_ctx_s::kMaxChunks - 1) / crisp_ctx_s::kMaxChunks);
   per = std::max(1, std::min(per, s.Hkv));
-  const int nchunks = (s.Hkv + per - 1) / per;
+  // Chunks (first KV head, KV heads, first query head, query heads, upload K/V).  With one
+  // KV head per chunk, the first and the last KV groups are split into one query head per
+  // chunk, so the upload before the first computation and the download after the last are
+  // one head's worth (the group's K/V travel with its first head).
+  struct Chunk {
+    int g0, m, h0, hn;
+    bool kv;
+  };
+  Chunk chunks[crisp_ctx_s::kMaxChunks];
+  int nchunks = 0;
+  const bool split_ends = per == 1 && group > 1 && s.Hkv >= 2 &&
+                          s.Hkv + 2 * (group - 1) <= crisp_ctx_s::kMaxChunks;
+  for (int g0 = 0; g0 < s.Hkv; g0 += per) {
+    const int m = std::min(per, s.Hkv - g0);
+    if (split_ends && (g0 == 0 || g0 == s.Hkv - 1)) {
+      for (int i = 0; i < group; ++i) chunks[nchunks++] = Chunk{g0, 1, g0 * group + i, 1, i == 0};
+    } else {
+      chunks[nchunks++] = Chunk{g0, m, g0 * group, m * group, true};
+    }
+  }
   const size_t head_bytes = static_cast<size_t>(s.n) * kD * 2;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   auto ok = [&](cudaError_t e, const char* what) { return launched(ctx, e, what) == CRISP_OK; };
@@ -399,21 +418,25 @@ crisp_status crisp_prefill_host(crisp_ctx ctx, const crisp_dims* dims, const voi
       !ok(cudaStreamWaitEvent(ctx->d2h, ctx->ev_entry, 0), "wait"))
     return CRISP_ERR_CUDA;
   for (int c = 0; c < nchunks; ++c) {
-    const int g0 = c * per, m = std::min(per, s.Hkv - g0), h0 = g0 * group;
-    const size_t qoff = static_cast<size_t>(h0) * head_bytes, kvoff = static_cast<size_t>(g0) * head_bytes;
-    const size_t qbytes = static_cast<size_t>(m) * group * head_bytes, kvbytes = static_cast<size_t>(m) * head_bytes;
+    const Chunk& ch = chunks[c];
+    const size_t qoff = static_cast<size_t>(ch.h0) * head_bytes;
+    const size_t kvoff = static_cast<size_t>(ch.g0) * head_bytes;
+    const size_t qbytes = static_cast<size_t>(ch.hn) * head_bytes;
+    const size_t kvbytes = static_cast<size_t>(ch.m) * head_bytes;
     // upload chunk c (the copy stream runs ahead of the compute stream)
     if (!ok(cudaMemcpyAsync(static_cast<char*>(Q) + qoff, static_cast<const char*>(Q_host) + qoff,
                             qbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload Q") ||
-        !ok(cudaMemcpyAsync(static_cast<char*>(K) + kvoff, static_cast<const char*>(K_host) + kvoff,
-                            kvbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload K") ||
-        !ok(cudaMemcpyAsync(static_cast<char*>(V) + kvoff, static_cast<const char*>(V_host) + kvoff,
-                            kvbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload V") ||
+        (ch.kv &&
+         (!ok(cudaMemcpyAsync(static_cast<char*>(K) + kvoff, static_cast<const char*>(K_host) + kvoff,
+                              kvbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload K") ||
+          !ok(cudaMemcpyAsync(static_cast<char*>(V) + kvoff, static_cast<const char*>(V_host) + kvoff,
+                              kvbytes, cudaMemcpyHostToDevice, ctx->h2d), "upload V"))) ||
         !ok(cudaEventRecord(ctx->ev_in[c], ctx->h2d), "record") ||
         !ok(cudaStreamWaitEvent(cs, ctx->ev_in[c], 0), "wait"))
       return CRISP_ERR_CUDA;
-    // select and attend chunk c: an independent problem of m KV heads
-    const crisp_dims sub{1, s.n, m * group, m, kD};
+    // select and attend chunk c: an independent problem of ch.hn query heads over ch.m KV
+    // heads
+    const crisp_dims sub{1, s.n, ch.hn, ch.m, kD};
     if ((st = crisp_select(ctx, &sub, static_cast<char*>(Q) + qoff, static_cast<char*>(K) + kvoff,
                            cfg, stream)) != CRISP_OK ||
         (st = crisp_attend(ctx, &sub, static_cast<char*>(Q) + qoff, static_cast<char*>(K) + kvoff,

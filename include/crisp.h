@@ -122,9 +122,11 @@ crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q,
 
 /* crisp_prefill from host memory, overlapping the copies with the work: the heads are
  * independent ("Method step details" runs steps 1-4 per head), so the call splits them
- * into chunks of whole KV-head groups and, per chunk, uploads Q, K, V (host -> the
- * caller's device buffers Q, K, V), selects and attends on `stream`, and downloads O
- * (-> O_host) while the next chunk is uploaded and computed.  Two copy streams owned by
+ * into chunks of whole KV-head groups (at long lengths the first and the last group go
+ * one query head per chunk, so that only one head's upload precedes the first
+ * computation and one head's download follows the last) and, per chunk, uploads Q, K, V
+ * (host -> the caller's device buffers Q, K, V), selects and attends on `stream`, and
+ * downloads O (-> O_host) while the next chunk is uploaded and computed.  Two copy streams owned by
  * the context carry the copies; events order them against `stream`, so synchronising
  * `stream` waits for everything, O_host included.  Host buffers should be page-locked
  * (cudaHostAlloc / cudaHostRegister) for the copies to overlap.  All eight buffers are

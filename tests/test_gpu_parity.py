@@ -286,6 +286,32 @@ def test_prefill_host_batch_two_uneven_chunks(dsp):
     ctx.close()
 
 
+def test_prefill_host_single_head_end_chunks(dsp):
+    """At 64k with 4 query heads per KV head, chunks hold one KV head and the first and
+    last groups are split into one query head per chunk (K/V uploaded with the group's
+    first head): the output must still match the device path."""
+    n, hq, hkv = 65536, 8, 2
+    g = random_qkv(n, hq, hkv, 128, seed=61, scale=3.0)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, n, hq, hkv)
+    ctx = dsp.Context(dims)
+    cfg = dsp.default_cfg()
+    o = torch.empty_like(q)
+    ctx.prefill(dims, q, k, v, cfg, o)
+    assert ctx.sync_status() == 0
+    ref = o.float().cpu().numpy().astype(np.float64)
+    t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = t(g["q"]), t(g["k"]), t(g["v"])
+    oh = torch.zeros(o.shape, dtype=torch.bfloat16).pin_memory()
+    q2, k2, v2, o2 = (torch.empty_like(x) for x in (q, k, v, o))
+    ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q2, k2, v2, o2)
+    assert ctx.sync_status() == 0
+    got = oh.float().numpy()
+    for h in range(hq):
+        compare_outputs(got[h], ref[h], f"prefill_host single-head chunks, head {h}")
+    ctx.close()
+
+
 def test_timeout_is_reported_and_context_recovers(dsp):
     """A dropped barrier arrive makes a bounded wait run out: the kernel exits, the host
     reads CRISP_ERR_TIMEOUT, and the next call on the same context succeeds."""
