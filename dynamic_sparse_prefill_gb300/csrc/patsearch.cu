@@ -177,30 +177,52 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
     for (int i = e; i < ntiles; i += 2) {
       if (!warp_wait(&s_full[e], (i >> 1) & 1, a.err, abort_flag, tmo)) break;
       tc_fence_after();
+      // The tile's S row in one TMEM load; the buffer goes straight back to the MMA warp.
+      uint32_t v[128];
+      tmem_ld128(row_taddr, v);
+      tc_fence_before();
+      mbar_arrive(&s_free[e]);
       const int t = t_begin + i;
       const bool last = (t == a.nb - 1);
       const int j0 = t * kBlk;
       // u: keys with c <= r (slash block N_b-1-t); w: keys with c > r (slash block
-      // N_b-2-t); the last tile is causal (c <= r only).
+      // N_b-2-t); the last tile is causal (c <= r only).  Column chunk c4 (32 keys) lies
+      // wholly left of the row's offset when c4 < q, wholly right when c4 > q; only the
+      // warp's own chunk c4 == q is split per lane.
       auto sums = [&](float m, float& u, float& w) {
-        float uu[4] = {0.f, 0.f, 0.f, 0.f}, ww[4] = {0.f, 0.f, 0.f, 0.f};
+        float ua = 0.f, ub = 0.f, wa = 0.f, wb = 0.f;
         const float neg = -m;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(row_taddr + c4 * 32, v);
+          if (c4 < q || (c4 > q && !last)) {
+            float sa = 0.f, sb = 0.f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = c4 * 32 + c;
-            const float x = fast_exp2(fmaf(__uint_as_float(v[c]), a.scale_log2, neg));
-            if (col <= r)
-              uu[c & 3] += x;
-            else if (!last)
-              ww[c & 3] += x;
+            for (int c = 0; c < 16; ++c) {
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(v[c4 * 32 + 2 * c]),
+                    __uint_as_float(v[c4 * 32 + 2 * c + 1]), a.scale_log2, a.scale_log2, neg, neg);
+              fadd2(sa, sb, sa, sb, fast_exp2(x0), fast_exp2(x1));
+            }
+            if (c4 < q) {
+              ua += sa;
+              ub += sb;
+            } else {
+              wa += sa;
+              wb += sb;
+            }
+          } else if (c4 == q) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float x = fast_exp2(fmaf(__uint_as_float(v[c4 * 32 + c]), a.scale_log2, neg));
+              if (c <= lane)
+                ua += x;
+              else if (!last)
+                wa += x;
+            }
           }
         }
-        u = (uu[0] + uu[1]) + (uu[2] + uu[3]);
-        w = (ww[0] + ww[1]) + (ww[2] + ww[3]);
+        u = ua + ub;
+        w = wa + wb;
       };
       float u = 0.f, w = 0.f;
       bool slow = !have_m;
@@ -213,13 +235,8 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx[k] = -FLT_MAX;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(row_taddr + c4 * 32, v);
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (!last || c4 * 32 + c <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
-        }
+        for (int c = 0; c < 128; ++c)
+          if (!last || c <= r) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
         const float ms = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
         if (!have_m || ms > m_run) m_run = ms;
@@ -231,21 +248,13 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       if (t == 0 || last) {
         const float neg = -m_run;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(row_taddr + c4 * 32, v);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = c4 * 32 + c;
-            const int j = j0 + col;
-            const bool valid = !last || col <= r;
-            const bool anchor = (t == 0 && j < a.w_sink) || (last && j >= a.n - a.w_local);
-            if (valid && anchor) an += fast_exp2(fmaf(__uint_as_float(v[c]), a.scale_log2, neg));
-          }
+        for (int c = 0; c < 128; ++c) {
+          const int j = j0 + c;
+          const bool valid = !last || c <= r;
+          const bool anchor = (t == 0 && j < a.w_sink) || (last && j >= a.n - a.w_local);
+          if (valid && anchor) an += fast_exp2(fmaf(__uint_as_float(v[c]), a.scale_log2, neg));
         }
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[e]);
       const size_t idx = (static_cast<size_t>(h) * a.nb + t) * kBlk + r;
       a.st_m[idx] = m_run;
       a.st_u[idx] = u;
@@ -645,9 +654,21 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   a.group = s.group;
   a.w_sink = cfg.w_sink;
   a.w_local = cfg.w_local;
-  // about three waves of CTAs over (head, tile chunk)
+  // About three waves of CTAs (one per SM) over (head, tile chunk): among the chunk
+  // counts near that, take the one whose last wave is fullest.
   const int want = max(1, (3 * ctx->num_sms + s.H - 1) / s.H);
-  const int chunks = min(s.nb, want);
+  int chunks = min(s.nb, want);
+  double best = -1.0;
+  for (int c = max(1, want / 2); c <= min(s.nb, 2 * want); ++c) {
+    const int tpc = (s.nb + c - 1) / c;
+    const int64_t ctas = static_cast<int64_t>(s.H) * ((s.nb + tpc - 1) / tpc);
+    const int64_t waves = (ctas + ctx->num_sms - 1) / ctx->num_sms;
+    const double fill = static_cast<double>(ctas) / static_cast<double>(waves * ctx->num_sms);
+    if (fill > best + 1e-9) {
+      best = fill;
+      chunks = c;
+    }
+  }
   a.tiles_per_cta = (s.nb + chunks - 1) / chunks;
   const int nchunks = (s.nb + a.tiles_per_cta - 1) / a.tiles_per_cta;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));

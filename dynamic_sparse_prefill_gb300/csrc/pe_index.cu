@@ -84,9 +84,10 @@ __global__ void __launch_bounds__(128) pe_pool_k_kernel(const uint16_t* __restri
 
 // ---------------------------------------------------------------- pooled logits
 // logits[I][K] = Qbar_I . Kbar_K / sqrt(d) for K <= I, in 128 x 128 tiles (fp32 FMA).  Each
-// thread accumulates 8 x 8 outputs (rows ty + 16i, columns tx + 16j), so a step over d
-// takes 16 shared-memory loads for 64 FMAs, and the loads of a warp fall in distinct banks
-// (the tiles are stored transposed, [d][row], with a row pitch of 129 floats).
+// thread accumulates 8 x 8 outputs (rows ty + 16i, columns tx + 16j), two columns per
+// packed f32x2 FMA, so a step over d takes 16 shared-memory loads and 32 FMA instructions,
+// and the loads of a warp fall in distinct banks (the tiles are stored transposed,
+// [d][row], with a row pitch of 129 floats).
 constexpr int kPT = 128;
 __global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict__ qbar,
                                                         const float* __restrict__ kbar,
@@ -99,11 +100,11 @@ __global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict_
   const int hk = (h / hq) * hkv + (h % hq) / group;
   __shared__ float sq[32][kPT + 1], sk[32][kPT + 1];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[8][8];
+  float2 acc[8][4];  // acc[i][j] = outputs (row ty + 16i, columns tx + 32j, tx + 32j + 16)
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
   for (int d0 = 0; d0 < kD; d0 += 32) {
     for (int i = threadIdx.x; i < kPT * 32; i += 256) {
       const int row = i >> 5, dd = i & 31;
@@ -114,25 +115,29 @@ __global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict_
     __syncthreads();
 #pragma unroll 4
     for (int dd = 0; dd < 32; ++dd) {
-      float a[8], b[8];
+      float a[8];
+      float2 b[4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = sq[dd][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = make_float2(sk[dd][tx + 32 * j], sk[dd][tx + 32 * j + 16]);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        a[i] = sq[dd][ty + 16 * i];
-        b[i] = sk[dd][tx + 16 * i];
+        const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int I = I0 + ty + 16 * i, K = K0 + tx + 16 * j;
-      if (I < nb && K <= I) pev[(static_cast<size_t>(h) * nb + I) * nb + K] = acc[i][j] * scale;
+    for (int j = 0; j < 4; ++j) {
+      const int I = I0 + ty + 16 * i, K = K0 + tx + 32 * j;
+      if (I < nb && K <= I) pev[(static_cast<size_t>(h) * nb + I) * nb + K] = acc[i][j].x * scale;
+      if (I < nb && K + 16 <= I)
+        pev[(static_cast<size_t>(h) * nb + I) * nb + K + 16] = acc[i][j].y * scale;
     }
 }
 
