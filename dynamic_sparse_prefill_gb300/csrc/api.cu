@@ -16,6 +16,7 @@
 namespace crisp {
 cudaError_t init_patsearch_attributes();
 cudaError_t init_attention_attributes();
+cudaError_t init_pe_attributes();
 }  // namespace crisp
 
 using namespace crisp;
@@ -217,7 +218,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
     return CRISP_ERR_CUDA;
   }
   ctx->encode = reinterpret_cast<EncodeTiledFn>(fn);
-  if (init_patsearch_attributes() != cudaSuccess || init_attention_attributes() != cudaSuccess) {
+  if (init_patsearch_attributes() != cudaSuccess || init_attention_attributes() != cudaSuccess ||
+      init_pe_attributes() != cudaSuccess) {
     delete ctx;
     return CRISP_ERR_CUDA;
   }
@@ -257,7 +259,8 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.counts), sizeof(int32_t) * H * 4},
       {reinterpret_cast<void**>(&w.selv), static_cast<size_t>(H * nb)},
       {reinterpret_cast<void**>(&w.sels), static_cast<size_t>(H * nb)},
-      {reinterpret_cast<void**>(&w.qbar), sizeof(float) * H * nb * kD},
+      {reinterpret_cast<void**>(&w.qs), sizeof(uint16_t) * 2 * H * nb * kD},
+      {reinterpret_cast<void**>(&w.ks), sizeof(uint16_t) * 2 * Hkv * nb * kD},
       {reinterpret_cast<void**>(&w.kbar), sizeof(float) * Hkv * nb * kD},
       {reinterpret_cast<void**>(&w.pev), sizeof(float) * H * nb * nb},
       {reinterpret_cast<void**>(&w.hist_cnt), sizeof(unsigned long long) * H * 256},
@@ -323,7 +326,12 @@ crisp_status crisp_select(crisp_ctx ctx, const crisp_dims* dims, const void* Q, 
   ctx->has_patsearch = false;
   if ((st = launched(ctx, launch_patsearch(ctx, s, *cfg, tmQ, tmK, cs), "patsearch")) != CRISP_OK)
     return st;
-  if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, cs), "pe_index")) != CRISP_OK)
+  CUtensorMap tmQs, tmKs;
+  if ((st = make_map3(ctx, &tmQs, ctx->ws.qs, 2 * static_cast<int64_t>(s.H) * s.nb)) != CRISP_OK ||
+      (st = make_map3(ctx, &tmKs, ctx->ws.ks, 2 * static_cast<int64_t>(s.Hkv) * s.nb)) != CRISP_OK)
+    return st;
+  if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, tmQs, tmKs, cs), "pe_index")) !=
+      CRISP_OK)
     return st;
   if ((st = launched(ctx, launch_build_csr(ctx, s, cs), "build_csr")) != CRISP_OK) return st;
   ctx->has_sel = true;

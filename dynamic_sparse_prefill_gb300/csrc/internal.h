@@ -49,9 +49,10 @@ struct Workspace {
   uint8_t* selv = nullptr;   // [H][nb]
   uint8_t* sels = nullptr;   // [H][nb]
   // PEIndex
-  float* qbar = nullptr;     // [H][nb][128]
-  float* kbar = nullptr;     // [Hkv][nb][128]
-  float* pev = nullptr;      // [H][nb][nb] pooled logits, then v = A_bar / N_b
+  uint16_t* qs = nullptr;    // [2][H*nb][128] bf16: Qbar * log2(e)/sqrt(d) as hi rows, then lo rows
+  uint16_t* ks = nullptr;    // [2][Hkv*nb][128] bf16: Kbar as hi rows, then lo rows
+  float* kbar = nullptr;     // [Hkv][nb][128] fp32 (JSD routing)
+  float* pev = nullptr;      // [H][nb][nb] v = A_bar / N_b (lower triangle)
   unsigned long long* hist_cnt = nullptr;  // [H][256]
   double* hist_mass = nullptr;             // [H][256]
   PeState* pe = nullptr;                   // [H]
@@ -112,8 +113,10 @@ Shape make_shape(const crisp_dims& d);
 // Each launcher only enqueues work on `st` and returns the launch status.
 cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
                              const CUtensorMap& tmQ, const CUtensorMap& tmK, cudaStream_t st);
+// tmQs/tmKs: 3-D maps (see make_map3) of ws.qs and ws.ks with 2*H*nb and 2*Hkv*nb rows.
 cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
-                            const void* K, cudaStream_t st);
+                            const void* K, const CUtensorMap& tmQs, const CUtensorMap& tmKs,
+                            cudaStream_t st);
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st);
 // KV heads per launch of the fast attention kernel (launch_attention splits the heads).
 int attention_kv_heads_per_launch(const Shape& s, int num_sms);

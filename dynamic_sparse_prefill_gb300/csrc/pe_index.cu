@@ -6,11 +6,15 @@
 // pooled scores, normalise and flatten, sort, and keep the top pairs until their
 // cumulative mass reaches gamma ("Prerequisites", the cumulative coverage rule).
 //
+// The pooled softmax runs on the tensor cores (pe_prob_kernel: the block means as bf16
+// hi/lo pairs, three MMA chains per tile, fp32 accumulate in TMEM) and writes v directly.
 // The sort is a radix select on the fp32 bit patterns of the (positive) flattened scores
 // with fp64 mass per digit: four 8-bit passes find the threshold value T with
 // mass(v > T) < gamma <= mass(v >= T); items equal to T are then taken in flat-index
 // order (I*N_b + K) until the running mass reaches gamma.  Every PE row also gets its
 // diagonal pair, so that no query block is left without keys.
+#include <cuda_bf16.h>
+
 #include <cfloat>
 
 #include "internal.h"
@@ -20,10 +24,26 @@ namespace crisp {
 namespace {
 
 // ---------------------------------------------------------------- block means
-// Qbar[h][I][:] = mean of the 128 rows of query block I (PE heads only).
+// The pooled logits Qbar_I . Kbar_K / sqrt(d) are formed on the tensor cores from bf16
+// pairs: x = hi + lo with hi = bf16(x) and lo = bf16(x - hi) (16 significant bits), and
+// Qbar . Kbar ~ hi_q.hi_k + hi_q.lo_k + lo_q.hi_k (the dropped lo.lo term and the split's
+// residue are ~2^-16 of |Qbar||Kbar|).  Qbar is scaled by log2(e)/sqrt(d) before the split,
+// so the product is the logit in base 2.  Layout: a [2][rows][128] bf16 plane pair
+// (hi rows first, then lo rows), rows = heads x N_b.
+__device__ __forceinline__ void split_store(uint16_t* hi_plane, size_t lo_offset, size_t idx,
+                                            float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+  hi_plane[idx] = __bfloat16_as_ushort(hi);
+  hi_plane[lo_offset + idx] = __bfloat16_as_ushort(lo);
+}
+
+// Qbar[h][I][:] = mean of the 128 rows of query block I (PE heads only), times
+// log2(e)/sqrt(d), split into bf16 pairs.
 __global__ void __launch_bounds__(128) pe_pool_q_kernel(const uint16_t* __restrict__ Q,
                                                         const uint8_t* __restrict__ route,
-                                                        int n, int nb, float* qbar) {
+                                                        int n, int nb, int H, float scale,
+                                                        uint16_t* qs) {
   const int h = blockIdx.y, I = blockIdx.x;
   if (route[h]) return;
   __shared__ float part[8][kD];
@@ -46,14 +66,15 @@ __global__ void __launch_bounds__(128) pe_pool_q_kernel(const uint16_t* __restri
   float s = 0.f;
 #pragma unroll
   for (int g = 0; g < 8; ++g) s += part[g][threadIdx.x];
-  qbar[(static_cast<size_t>(h) * nb + I) * kD + threadIdx.x] = s * (1.f / kBlk);
+  split_store(qs, static_cast<size_t>(H) * nb * kD,
+              (static_cast<size_t>(h) * nb + I) * kD + threadIdx.x, s * (1.f / kBlk) * scale);
 }
 
-// Kbar for every KV head that serves at least one PE query head.
+// Kbar for every KV head that serves at least one PE query head, split into bf16 pairs.
 __global__ void __launch_bounds__(128) pe_pool_k_kernel(const uint16_t* __restrict__ K,
                                                         const uint8_t* __restrict__ route,
                                                         int n, int nb, int hq, int hkv,
-                                                        int group, float* kbar) {
+                                                        int group, int Hkv, uint16_t* ks) {
   const int hk = blockIdx.y, I = blockIdx.x;
   const int bidx = hk / hkv, kvh = hk % hkv;
   bool any_pe = false;
@@ -79,105 +100,275 @@ __global__ void __launch_bounds__(128) pe_pool_k_kernel(const uint16_t* __restri
   float s = 0.f;
 #pragma unroll
   for (int g = 0; g < 8; ++g) s += part[g][threadIdx.x];
-  kbar[(static_cast<size_t>(hk) * nb + I) * kD + threadIdx.x] = s * (1.f / kBlk);
+  split_store(ks, static_cast<size_t>(Hkv) * nb * kD,
+              (static_cast<size_t>(hk) * nb + I) * kD + threadIdx.x, s * (1.f / kBlk));
 }
 
-// ---------------------------------------------------------------- pooled logits
-// logits[I][K] = Qbar_I . Kbar_K / sqrt(d) for K <= I, in 128 x 128 tiles (fp32 FMA).  Each
-// thread accumulates 8 x 8 outputs (rows ty + 16i, columns tx + 16j), two columns per
-// packed f32x2 FMA, so a step over d takes 16 shared-memory loads and 32 FMA instructions,
-// and the loads of a warp fall in distinct banks (the tiles are stored transposed,
-// [d][row], with a row pitch of 129 floats).
-constexpr int kPT = 128;
-__global__ void __launch_bounds__(256) pe_scores_kernel(const float* __restrict__ qbar,
-                                                        const float* __restrict__ kbar,
-                                                        const uint8_t* __restrict__ route,
-                                                        int nb, int hq, int hkv, int group,
-                                                        float scale, float* pev) {
-  const int h = blockIdx.z;
-  const int I0 = blockIdx.y * kPT, K0 = blockIdx.x * kPT;
-  if (route[h] || K0 > I0 + kPT - 1) return;
-  const int hk = (h / hq) * hkv + (h % hq) / group;
-  __shared__ float sq[32][kPT + 1], sk[32][kPT + 1];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float2 acc[8][4];  // acc[i][j] = outputs (row ty + 16i, columns tx + 32j, tx + 32j + 16)
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
-  for (int d0 = 0; d0 < kD; d0 += 32) {
-    for (int i = threadIdx.x; i < kPT * 32; i += 256) {
-      const int row = i >> 5, dd = i & 31;
-      const int I = I0 + row, K = K0 + row;
-      sq[dd][row] = I < nb ? qbar[(static_cast<size_t>(h) * nb + I) * kD + d0 + dd] : 0.f;
-      sk[dd][row] = K < nb ? kbar[(static_cast<size_t>(hk) * nb + K) * kD + d0 + dd] : 0.f;
+// ---------------------------------------------------------------- pooled softmax
+// v[I][K] = softmax_{K <= I}(Qbar_I . Kbar_K / sqrt(d)) / N_b for one PE head and one tile
+// of 128 query blocks I (row tile t), written row-major into the head's N_b x N_b square.
+//
+// One CTA per (head, row tile), longest rows first.  Warp 0 loads the row tile's Qbar pair
+// once and streams the Kbar pairs of key tiles 0..t twice through a 2-stage ring (TMA, one
+// 3-D copy per 32 KB plane tile); warp 1 issues three bf16 MMA chains per key tile
+// (hi.hi + hi.lo + lo.hi, M = N = 128, K = 128) into one of two TMEM S buffers; warps 2-9
+// are two warpgroups that take alternate key tiles, thread <-> row (TMEM lane).  Pass 0
+// (the first t+1 jobs) keeps each row's running maximum and sum of 2^(s - m); the two
+// warpgroups then merge their partial (m, sum) per row through shared memory; pass 1 (the
+// next t+1 jobs, same MMAs) writes 2^(s - M) / (Z N_b).  Writes go through a 32 x 32
+// per-warp staging tile so that each store instruction covers 32 consecutive keys of one
+// row.  The diagonal tile keeps keys K <= I; rows I >= N_b are dropped.
+constexpr int kPeThreads = 320;
+constexpr int kPeBStages = 2;
+constexpr uint32_t kIdescPe = idesc_bf16_f32(128, 128, false, false);
+constexpr int kPeStagePerWarp = 32 * 17;  // floats
+constexpr size_t kPeStageBytes = 8 * kPeStagePerWarp * sizeof(float);
+constexpr size_t kPeSmem = 2 * kTileBytes + kPeBStages * 2 * kTileBytes + kPeStageBytes +
+                           2 * kBlk * sizeof(float2) + 256;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort, uint64_t tmo) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, abort, tmo) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                           uint64_t tmo) {
+  volatile int never = 0;
+  mbar_wait(bar, parity, err, &never, tmo);
+}
+
+struct PeProbArgs {
+  const uint8_t* route;
+  int nb, nt, hq, hkv, group;
+  int q_lo_rows;  // row offset of the lo plane in the Qbar map (heads x N_b)
+  int k_lo_rows;  // same for the Kbar map
+  float inv_nb;
+  float* pev;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(kPeThreads, 1)
+    pe_prob_kernel(const __grid_constant__ CUtensorMap tmQs,
+                   const __grid_constant__ CUtensorMap tmKs, const PeProbArgs a) {
+  const int h = blockIdx.x;
+  if (a.route[h]) return;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrRange);
+    return;
+  }
+  const int t = a.nt - 1 - static_cast<int>(blockIdx.y);  // row tile
+  const int T = t + 1;                                    // key tiles 0..t
+  const int jobs = 2 * T;                                 // pass 0, then pass 1
+  uint8_t* sA = smem_raw;                                 // Qbar hi | lo
+  uint8_t* sB = sA + 2 * kTileBytes;                      // per stage: Kbar hi | lo
+  float* stage = reinterpret_cast<float*>(sB + kPeBStages * 2 * kTileBytes);
+  float2* xchg = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(stage) + kPeStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xchg + 2 * kBlk);
+  uint64_t* a_full = bars;
+  uint64_t* b_full = bars + 1;   // [kPeBStages]
+  uint64_t* b_empty = bars + 3;  // [kPeBStages]
+  uint64_t* s_full = bars + 5;   // [2]
+  uint64_t* s_free = bars + 7;   // [2]
+  uint64_t* x_ready = bars + 9;  // both warpgroups' pass-0 row statistics are in xchg
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hk = (h / a.hq) * a.hkv + (h % a.hq) / a.group;
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    for (int s = 0; s < kPeBStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
-    __syncthreads();
-#pragma unroll 4
-    for (int dd = 0; dd < 32; ++dd) {
-      float a[8];
-      float2 b[4];
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(x_ready, 256);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQs);
+      tma_prefetch_desc(&tmKs);
+      const int qrow = h * a.nb + t * kBlk;
+      mbar_arrive_expect_tx(a_full, 2 * kTileBytes);
+      tma_load_3d(sA, &tmQs, a_full, 0, qrow, 0);
+      tma_load_3d(sA + kTileBytes, &tmQs, a_full, 0, a.q_lo_rows + qrow, 0);
+      int issued = 0;
+      for (int j = 0; j < jobs; ++j) {
+        const int s = j & 1;
+        if (j >= kPeBStages &&
+            !mbar_wait(&b_empty[s], ((j >> 1) + 1) & 1, a.err, abort_flag, tmo))
+          break;
+        const int krow = hk * a.nb + (j < T ? j : j - T) * kBlk;
+        uint8_t* dst = sB + s * 2 * kTileBytes;
+        mbar_arrive_expect_tx(&b_full[s], 2 * kTileBytes);
+        tma_load_3d(dst, &tmKs, &b_full[s], 0, krow, 0);
+        tma_load_3d(dst + kTileBytes, &tmKs, &b_full[s], 0, a.k_lo_rows + krow, 0);
+        ++issued;
+      }
+      drain_wait(a_full, 0, a.err, tmo);
+      for (int j = max(0, issued - kPeBStages); j < issued; ++j)
+        drain_wait(&b_full[j & 1], (j >> 1) & 1, a.err, tmo);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (mbar_wait(a_full, 0, a.err, abort_flag, tmo)) {
+        const uint32_t a_hi = smem_u32(sA), a_lo = a_hi + kTileBytes;
+        for (int j = 0; j < jobs; ++j) {
+          const int s = j & 1;  // B stage and S buffer
+          if (!mbar_wait(&b_full[s], (j >> 1) & 1, a.err, abort_flag, tmo)) break;
+          if (j >= 2 && !mbar_wait(&s_free[s], ((j >> 1) + 1) & 1, a.err, abort_flag, tmo))
+            break;
+          tc_fence_after();
+          const uint32_t b_hi = smem_u32(sB + s * 2 * kTileBytes), b_lo = b_hi + kTileBytes;
+          const uint32_t d = tmem + s * 128;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = sq[dd][ty + 16 * i];
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+            umma_bf16(d, sdesc_sw128(a_hi + off, 16, 1024), sdesc_sw128(b_hi + off, 16, 1024),
+                      kIdescPe, kk > 0 ? 1u : 0u);
+            umma_bf16(d, sdesc_sw128(a_hi + off, 16, 1024), sdesc_sw128(b_lo + off, 16, 1024),
+                      kIdescPe, 1u);
+            umma_bf16(d, sdesc_sw128(a_lo + off, 16, 1024), sdesc_sw128(b_hi + off, 16, 1024),
+                      kIdescPe, 1u);
+          }
+          umma_commit(&s_full[s]);
+          umma_commit(&b_empty[s]);
+        }
+      }
+      umma_commit(drain);
+      drain_wait(drain, 0, a.err, tmo);
+    }
+  } else {
+    const int e = (warp - 2) >> 2;  // warpgroup: jobs j with (j & 1) == e, S buffer e
+    const int q = warp & 3;         // TMEM lane quarter
+    const int r = q * 32 + lane;
+    const int I = t * kBlk + r;
+    const bool row_ok = I < a.nb;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + e * 128;
+    bool ok = true;
+    float m_run = -FLT_MAX, z = 0.f;
+    for (int j = e; j < T; j += 2) {
+      if (!warp_wait(&s_full[e], (j >> 1) & 1, a.err, abort_flag, tmo)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[128];
+      tmem_ld128(taddr, v);
+      tc_fence_before();
+      mbar_arrive(&s_free[e]);
+      const int lim = row_ok ? (j == t ? r : kBlk - 1) : -1;  // keys c <= lim are in the row
+      if (lim == kBlk - 1) {
+        float mx[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = make_float2(sk[dd][tx + 32 * j], sk[dd][tx + 32 * j + 16]);
+        for (int k = 0; k < 8; ++k) mx[k] = -FLT_MAX;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 ai = make_float2(a[i], a[i]);
+        for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mn = fmaxf(m_run, mt);
+        float sa = 0.f, sb = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
+        for (int c = 0; c < 64; ++c) {
+          float x0, x1;
+          fadd2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), -mn, -mn);
+          fadd2(sa, sb, sa, sb, fast_exp2(x0), fast_exp2(x1));
+        }
+        z = z * fast_exp2(m_run - mn) + (sa + sb);
+        m_run = mn;
+      } else if (lim >= 0) {
+        float mt = -FLT_MAX;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c <= lim) mt = fmaxf(mt, __uint_as_float(v[c]));
+        const float mn = fmaxf(m_run, mt);
+        float sa = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c <= lim) sa += fast_exp2(__uint_as_float(v[c]) - mn);
+        z = z * fast_exp2(m_run - mn) + sa;
+        m_run = mn;
       }
     }
-    __syncthreads();
-  }
+    // Merge the two warpgroups' row statistics (every epilogue thread arrives once).
+    xchg[e * kBlk + r] = make_float2(m_run, z);
+    mbar_arrive(x_ready);
+    ok = warp_wait(x_ready, 0, a.err, abort_flag, tmo) && ok;
+    if (ok) {
+      const float2 p0 = xchg[r], p1 = xchg[kBlk + r];
+      const float M = fmaxf(p0.x, p1.x);
+      const float Z = p0.y * fast_exp2(p0.x - M) + p1.y * fast_exp2(p1.x - M);
+      const float inv = a.inv_nb / Z;
+      float* st = stage + (warp - 2) * kPeStagePerWarp;  // [32 rows][16 keys], row pitch 17
+      float* out = a.pev + static_cast<size_t>(h) * a.nb * a.nb;
+      const int half = lane >> 4, col = lane & 15;
+      for (int j = T + ((T & 1) != e ? 1 : 0); j < jobs; j += 2) {
+        if (!warp_wait(&s_full[e], (j >> 1) & 1, a.err, abort_flag, tmo)) break;
+        tc_fence_after();
+        uint32_t v[128];
+        tmem_ld128(taddr, v);
+        tc_fence_before();
+        mbar_arrive(&s_free[e]);
+        const int kt = j - T;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+        for (int c16 = 0; c16 < 8; ++c16) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int I = I0 + ty + 16 * i, K = K0 + tx + 32 * j;
-      if (I < nb && K <= I) pev[(static_cast<size_t>(h) * nb + I) * nb + K] = acc[i][j].x * scale;
-      if (I < nb && K + 16 <= I)
-        pev[(static_cast<size_t>(h) * nb + I) * nb + K + 16] = acc[i][j].y * scale;
+          for (int c = 0; c < 16; c += 2) {
+            float x0, x1, y0, y1;
+            fadd2(x0, x1, __uint_as_float(v[c16 * 16 + c]), __uint_as_float(v[c16 * 16 + c + 1]),
+                  -M, -M);
+            ffma2(y0, y1, fast_exp2(x0), fast_exp2(x1), inv, inv, 0.f, 0.f);
+            st[lane * 17 + c] = y0;
+            st[lane * 17 + c + 1] = y1;
+          }
+          __syncwarp();
+          // lanes 0-15 store 16 keys of row rr, lanes 16-31 those of row rr + 1
+          const int K = kt * kBlk + c16 * 16 + col;
+#pragma unroll 4
+          for (int rr = 0; rr < 32; rr += 2) {
+            const int row = rr + half;
+            const int Ir = t * kBlk + q * 32 + row;
+            const float y = st[row * 17 + col];
+            if (Ir < a.nb && K <= Ir) out[static_cast<size_t>(Ir) * a.nb + K] = y;
+          }
+          __syncwarp();
+        }
+      }
     }
-}
-
-// v[I][K] = softmax_{K <= I}(logits[I]) / N_b, in place.
-__global__ void __launch_bounds__(256) pe_softmax_kernel(const uint8_t* __restrict__ route,
-                                                         int nb, float* pev) {
-  const int h = blockIdx.y, I = blockIdx.x;
-  if (route[h]) return;
-  __shared__ float red[8];
-  __shared__ float bc;
-  float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
-  const int len = I + 1;
-  float mx = -FLT_MAX;
-  for (int K = threadIdx.x; K < len; K += 256) mx = fmaxf(mx, row[K]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = red[0];
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
-    bc = m;
   }
+  tc_fence_before();
   __syncthreads();
-  mx = bc;
-  float s = 0.f;
-  for (int K = threadIdx.x; K < len; K += 256) s += expf(row[K] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int i = 0; i < 8; ++i) t += red[i];
-    bc = 1.f / (t * static_cast<float>(nb));
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
-  __syncthreads();
-  const float inv = bc;
-  for (int K = threadIdx.x; K < len; K += 256) row[K] = expf(row[K] - mx) * inv;
 }
 
 // ---------------------------------------------------------------- radix select
@@ -462,19 +653,35 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
 
 }  // namespace
 
+cudaError_t init_pe_attributes() {
+  return cudaFuncSetAttribute(pe_prob_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kPeSmem));
+}
+
 cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
-                            const void* K, cudaStream_t st) {
+                            const void* K, const CUtensorMap& tmQs, const CUtensorMap& tmKs,
+                            cudaStream_t st) {
   Workspace& w = ctx->ws;
   const uint16_t* q = static_cast<const uint16_t*>(Q);
   const uint16_t* k = static_cast<const uint16_t*>(K);
-  pe_pool_q_kernel<<<dim3(s.nb, s.H), 128, 0, st>>>(q, w.route, s.n, s.nb, w.qbar);
+  pe_pool_q_kernel<<<dim3(s.nb, s.H), 128, 0, st>>>(
+      q, w.route, s.n, s.nb, s.H, 1.4426950408889634f / sqrtf(static_cast<float>(kD)), w.qs);
   pe_pool_k_kernel<<<dim3(s.nb, s.Hkv), 128, 0, st>>>(k, w.route, s.n, s.nb, s.hq, s.hkv,
-                                                       s.group, w.kbar);
-  const int nt = (s.nb + kPT - 1) / kPT;
-  pe_scores_kernel<<<dim3(nt, nt, s.H), 256, 0, st>>>(w.qbar, w.kbar, w.route, s.nb, s.hq,
-                                                      s.hkv, s.group,
-                                                      1.f / sqrtf(static_cast<float>(kD)), w.pev);
-  pe_softmax_kernel<<<dim3(s.nb, s.H), 256, 0, st>>>(w.route, s.nb, w.pev);
+                                                       s.group, s.Hkv, w.ks);
+  PeProbArgs pa;
+  pa.route = w.route;
+  pa.nb = s.nb;
+  pa.nt = (s.nb + kBlk - 1) / kBlk;
+  pa.hq = s.hq;
+  pa.hkv = s.hkv;
+  pa.group = s.group;
+  pa.q_lo_rows = s.H * s.nb;
+  pa.k_lo_rows = s.Hkv * s.nb;
+  pa.inv_nb = 1.f / static_cast<float>(s.nb);
+  pa.pev = w.pev;
+  pa.err = w.err;
+  pa.timeout_ns = ctx->timeout_ns;
+  pe_prob_kernel<<<dim3(s.H, pa.nt), kPeThreads, kPeSmem, st>>>(tmQs, tmKs, pa);
   pe_radix_init_kernel<<<s.H, 256, 0, st>>>(w.pe, w.hist_cnt, w.hist_mass);
   for (int pass = 0; pass < 4; ++pass) {
     pe_hist_kernel<<<dim3((s.nb + kHistRows - 1) / kHistRows, s.H), 256, 0, st>>>(
