@@ -101,6 +101,28 @@ crisp_status make_map3(crisp_ctx ctx, CUtensorMap* map, const void* base, int64_
   return CRISP_OK;
 }
 
+// The PE probability triangle v as an fp32 tensor {nb keys, nb rows, H heads} (row pitch
+// nb * 4 bytes, a multiple of 16 when nb % 4 == 0), stored in boxes of 16 keys x 32 rows
+// from a 64-byte swizzled shared-memory tile.
+crisp_status make_prob_map(crisp_ctx ctx, CUtensorMap* map, const void* base, int64_t nb,
+                           int64_t heads) {
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(nb),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(nb) * 4, static_cast<cuuint64_t>(nb * nb) * 4};
+  cuuint32_t box[3] = {16, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
+                           gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(ctx->last_err, sizeof(ctx->last_err), "cuTensorMapEncodeTiled (fp32) failed (%d)",
+             static_cast<int>(r));
+    return CRISP_ERR_CUDA;
+  }
+  return CRISP_OK;
+}
+
 crisp_status launched(crisp_ctx ctx, cudaError_t e, const char* what) {
   if (e == cudaSuccess) return CRISP_OK;
   set_err(ctx, what, e);
@@ -330,8 +352,12 @@ crisp_status crisp_select(crisp_ctx ctx, const crisp_dims* dims, const void* Q, 
   if ((st = make_map3(ctx, &tmQs, ctx->ws.qs, 2 * static_cast<int64_t>(s.H) * s.nb)) != CRISP_OK ||
       (st = make_map3(ctx, &tmKs, ctx->ws.ks, 2 * static_cast<int64_t>(s.Hkv) * s.nb)) != CRISP_OK)
     return st;
-  if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, tmQs, tmKs, cs), "pe_index")) !=
-      CRISP_OK)
+  CUtensorMap tmO;
+  memset(&tmO, 0, sizeof(tmO));
+  const bool tma_out = (s.nb % 4) == 0;
+  if (tma_out && (st = make_prob_map(ctx, &tmO, ctx->ws.pev, s.nb, s.H)) != CRISP_OK) return st;
+  if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, tmQs, tmKs, tmO, tma_out, cs),
+                     "pe_index")) != CRISP_OK)
     return st;
   if ((st = launched(ctx, launch_build_csr(ctx, s, cs), "build_csr")) != CRISP_OK) return st;
   ctx->has_sel = true;

@@ -113,10 +113,12 @@ Shape make_shape(const crisp_dims& d);
 // Each launcher only enqueues work on `st` and returns the launch status.
 cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
                              const CUtensorMap& tmQ, const CUtensorMap& tmK, cudaStream_t st);
-// tmQs/tmKs: 3-D maps (see make_map3) of ws.qs and ws.ks with 2*H*nb and 2*Hkv*nb rows.
+// tmQs/tmKs: 3-D maps (see make_map3) of ws.qs and ws.ks with 2*H*nb and 2*Hkv*nb rows;
+// tmO: fp32 map of ws.pev, dims {nb, nb, H}, box {16, 32, 1}, 64-byte swizzle, valid when
+// tma_out (nb % 4 == 0).
 cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
                             const void* K, const CUtensorMap& tmQs, const CUtensorMap& tmKs,
-                            cudaStream_t st);
+                            const CUtensorMap& tmO, bool tma_out, cudaStream_t st);
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st);
 // KV heads per launch of the fast attention kernel (launch_attention splits the heads).
 int attention_kv_heads_per_launch(const Shape& s, int num_sms);

@@ -115,14 +115,18 @@ __global__ void __launch_bounds__(128) pe_pool_k_kernel(const uint16_t* __restri
 // are two warpgroups that take alternate key tiles, thread <-> row (TMEM lane).  Pass 0
 // (the first t+1 jobs) keeps each row's running maximum and sum of 2^(s - m); the two
 // warpgroups then merge their partial (m, sum) per row through shared memory; pass 1 (the
-// next t+1 jobs, same MMAs) writes 2^(s - M) / (Z N_b).  Writes go through a 32 x 32
-// per-warp staging tile so that each store instruction covers 32 consecutive keys of one
-// row.  The diagonal tile keeps keys K <= I; rows I >= N_b are dropped.
+// next t+1 jobs, same MMAs) writes 2^(s - M) / (Z N_b).  Each epilogue warp stages its 32
+// rows 16 keys at a time in shared memory and lane 0 hands the box to a TMA store (3-D
+// map {N_b, N_b, heads}: rows and keys past N_b are clipped by the copy); the diagonal
+// tile's keys K > I are written as 0 (never read).  Without the map (N_b % 4 != 0: row
+// pitch not a multiple of 16 bytes) the warp stores through a pitch-17 staging tile,
+// 16 consecutive keys of two rows per instruction, keys K <= I only.
 constexpr int kPeThreads = 320;
 constexpr int kPeBStages = 2;
 constexpr uint32_t kIdescPe = idesc_bf16_f32(128, 128, false, false);
-constexpr int kPeStagePerWarp = 32 * 17;  // floats
-constexpr size_t kPeStageBytes = 8 * kPeStagePerWarp * sizeof(float);
+constexpr int kPeStagePerWarp = 32 * 17;   // floats (store path without TMA)
+constexpr int kPeBoxBytes = 32 * 16 * 4;    // one TMA store box: 32 rows x 16 keys
+constexpr size_t kPeStageBytes = 8 * 2 * kPeBoxBytes;  // two boxes per epilogue warp
 constexpr size_t kPeSmem = 2 * kTileBytes + kPeBStages * 2 * kTileBytes + kPeStageBytes +
                            2 * kBlk * sizeof(float2) + 256;
 
@@ -151,6 +155,7 @@ struct PeProbArgs {
   int q_lo_rows;  // row offset of the lo plane in the Qbar map (heads x N_b)
   int k_lo_rows;  // same for the Kbar map
   float inv_nb;
+  int tma_out;  // 1: v leaves through TMA stores (tmO valid: N_b % 4 == 0)
   float* pev;
   uint32_t* err;
   uint64_t timeout_ns;
@@ -158,7 +163,8 @@ struct PeProbArgs {
 
 __global__ void __launch_bounds__(kPeThreads, 1)
     pe_prob_kernel(const __grid_constant__ CUtensorMap tmQs,
-                   const __grid_constant__ CUtensorMap tmKs, const PeProbArgs a) {
+                   const __grid_constant__ CUtensorMap tmKs,
+                   const __grid_constant__ CUtensorMap tmO, const PeProbArgs a) {
   const int h = blockIdx.x;
   if (a.route[h]) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -326,9 +332,14 @@ __global__ void __launch_bounds__(kPeThreads, 1)
       const float M = fmaxf(p0.x, p1.x);
       const float Z = p0.y * fast_exp2(p0.x - M) + p1.y * fast_exp2(p1.x - M);
       const float inv = a.inv_nb / Z;
-      float* st = stage + (warp - 2) * kPeStagePerWarp;  // [32 rows][16 keys], row pitch 17
       float* out = a.pev + static_cast<size_t>(h) * a.nb * a.nb;
       const int half = lane >> 4, col = lane & 15;
+      // TMA path: per warp two 2 KB boxes [32 rows][16 keys] in the 64-byte swizzled layout
+      // (16-byte chunk i of row rr at chunk i ^ ((rr >> 1) & 3)), stored by lane 0.
+      uint8_t* box = reinterpret_cast<uint8_t*>(stage) + (warp - 2) * 2 * kPeBoxBytes;
+      // Fallback: a [32 rows][16 keys] tile with row pitch 17, stored by the whole warp.
+      float* st = stage + (warp - 2) * kPeStagePerWarp;
+      int nbox = 0;
       for (int j = T + ((T & 1) != e ? 1 : 0); j < jobs; j += 2) {
         if (!warp_wait(&s_full[e], (j >> 1) & 1, a.err, abort_flag, tmo)) break;
         tc_fence_after();
@@ -337,30 +348,52 @@ __global__ void __launch_bounds__(kPeThreads, 1)
         tc_fence_before();
         mbar_arrive(&s_free[e]);
         const int kt = j - T;
+        const int lim = kt == t ? r : kBlk - 1;  // keys c <= lim are in the row (diagonal tile)
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16) {
+          float y[16];
 #pragma unroll
           for (int c = 0; c < 16; c += 2) {
-            float x0, x1, y0, y1;
+            float x0, x1;
             fadd2(x0, x1, __uint_as_float(v[c16 * 16 + c]), __uint_as_float(v[c16 * 16 + c + 1]),
                   -M, -M);
-            ffma2(y0, y1, fast_exp2(x0), fast_exp2(x1), inv, inv, 0.f, 0.f);
-            st[lane * 17 + c] = y0;
-            st[lane * 17 + c + 1] = y1;
+            ffma2(y[c], y[c + 1], fast_exp2(x0), fast_exp2(x1), inv, inv, 0.f, 0.f);
+            if (c16 * 16 + c > lim) y[c] = 0.f;
+            if (c16 * 16 + c + 1 > lim) y[c + 1] = 0.f;
           }
-          __syncwarp();
-          // lanes 0-15 store 16 keys of row rr, lanes 16-31 those of row rr + 1
-          const int K = kt * kBlk + c16 * 16 + col;
+          if (a.tma_out) {
+            uint8_t* b = box + (nbox & 1) * kPeBoxBytes;
+            if (lane == 0 && nbox >= 2) bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<float4*>(b + lane * 64 + 16 * (i ^ ((lane >> 1) & 3))) =
+                  make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmO, b, kt * kBlk + c16 * 16, t * kBlk + q * 32, h);
+              bulk_commit_group();
+            }
+            ++nbox;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) st[lane * 17 + c] = y[c];
+            __syncwarp();
+            // lanes 0-15 store 16 keys of row rr, lanes 16-31 those of row rr + 1
+            const int K = kt * kBlk + c16 * 16 + col;
 #pragma unroll 4
-          for (int rr = 0; rr < 32; rr += 2) {
-            const int row = rr + half;
-            const int Ir = t * kBlk + q * 32 + row;
-            const float y = st[row * 17 + col];
-            if (Ir < a.nb && K <= Ir) out[static_cast<size_t>(Ir) * a.nb + K] = y;
+            for (int rr = 0; rr < 32; rr += 2) {
+              const int row = rr + half;
+              const int Ir = t * kBlk + q * 32 + row;
+              const float yv = st[row * 17 + col];
+              if (Ir < a.nb && K <= Ir) out[static_cast<size_t>(Ir) * a.nb + K] = yv;
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
+      if (lane == 0 && nbox > 0) bulk_wait_group<0>();
     }
   }
   tc_fence_before();
@@ -660,7 +693,7 @@ cudaError_t init_pe_attributes() {
 
 cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
                             const void* K, const CUtensorMap& tmQs, const CUtensorMap& tmKs,
-                            cudaStream_t st) {
+                            const CUtensorMap& tmO, bool tma_out, cudaStream_t st) {
   Workspace& w = ctx->ws;
   const uint16_t* q = static_cast<const uint16_t*>(Q);
   const uint16_t* k = static_cast<const uint16_t*>(K);
@@ -681,7 +714,8 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
   pa.pev = w.pev;
   pa.err = w.err;
   pa.timeout_ns = ctx->timeout_ns;
-  pe_prob_kernel<<<dim3(s.H, pa.nt), kPeThreads, kPeSmem, st>>>(tmQs, tmKs, pa);
+  pa.tma_out = tma_out ? 1 : 0;
+  pe_prob_kernel<<<dim3(s.H, pa.nt), kPeThreads, kPeSmem, st>>>(tmQs, tmKs, tmO, pa);
   pe_radix_init_kernel<<<s.H, 256, 0, st>>>(w.pe, w.hist_cnt, w.hist_mass);
   for (int pass = 0; pass < 4; ++pass) {
     pe_hist_kernel<<<dim3((s.nb + kHistRows - 1) / kHistRows, s.H), 256, 0, st>>>(

@@ -131,6 +131,17 @@ def test_edge_shapes_random(dsp, n, hq, hkv, seed):
         run_parity(dsp, w, g, flags=flags)
 
 
+@pytest.mark.parametrize("n,hq,hkv,seed", [(512, 2, 1, 6), (16896, 2, 1, 7)])
+def test_edge_shapes_clipped_prob_stores(dsp, n, hq, hkv, seed):
+    """N_b = 4 and 132 (N_b % 4 == 0, so the PE probabilities leave through TMA stores whose
+    boxes run past the last row and key: the copy must clip them), both routes forced;
+    full selection parity, outputs on sampled query blocks."""
+    g = random_qkv(n, hq, hkv, 128, seed, scale=3.0)
+    w = Workload("edge_tma", n=n, hq=hq, hkv=hkv, seed=seed)
+    for flags in (dsp.FLAG_FORCE_PE, 0):
+        run_parity(dsp, w, g, sample=(hq, 6), seed=seed, flags=flags)
+
+
 @pytest.mark.parametrize("alpha,kmin,gamma", [(0.0, 0, 0.5), (1.25, 0, 0.95), (1.0, 4096, 1.0),
                                               (3.0, 256, 0.99)])
 def test_parameter_edges(dsp, alpha, kmin, gamma):
