@@ -59,8 +59,9 @@ __global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restri
   }
 }
 
-// Counts the blocks of 1024 rows (a warp per row) and scans them inside the CTA:
-// row_ptr[row] = offset within the CTA's rows, blk[b] = the CTA's total.
+// Counts the blocks of 1024 rows (a warp per row, or a thread per row when a row mask is
+// at most 16 words) and scans them inside the CTA: row_ptr[row] = offset within the CTA's
+// rows, blk[b] = the CTA's total.
 __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __restrict__ rowmask,
                                                               int64_t rows, int nbw,
                                                               int64_t* row_ptr, int64_t* blk) {
@@ -68,16 +69,26 @@ __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __
   __shared__ int wsum[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 1024;
-  for (int i = warp; i < 1024; i += 32) {
-    const int64_t row = r0 + i;
+  if (nbw <= 16) {
+    const int64_t row = r0 + threadIdx.x;
     int c = 0;
     if (row < rows) {
       const uint32_t* m = rowmask + row * nbw;
-      for (int wd = lane; wd < nbw; wd += 32) c += __popc(m[wd]);
+      for (int wd = 0; wd < nbw; ++wd) c += __popc(m[wd]);
     }
+    cnt[threadIdx.x] = c;
+  } else {
+    for (int i = warp; i < 1024; i += 32) {
+      const int64_t row = r0 + i;
+      int c = 0;
+      if (row < rows) {
+        const uint32_t* m = rowmask + row * nbw;
+        for (int wd = lane; wd < nbw; wd += 32) c += __popc(m[wd]);
+      }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (lane == 0) cnt[i] = c;
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0) cnt[i] = c;
+    }
   }
   __syncthreads();
   const int c = cnt[threadIdx.x];

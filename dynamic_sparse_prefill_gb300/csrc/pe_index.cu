@@ -416,11 +416,15 @@ __global__ void pe_radix_init_kernel(PeState* pe, unsigned long long* hist_cnt,
   hist_mass[h * 256 + threadIdx.x] = 0.0;
 }
 
-constexpr int kHistRows = 16;
+// Rows of the PE triangle per histogram CTA: 16 long rows, fewer short ones, so that short
+// triangles still spread over many CTAs (each CTA walks its rows one after the other).
+int hist_rows_per_cta(int nb) { return nb >= 1024 ? 16 : (nb >= 256 ? 4 : 1); }
+
 __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ pev,
                                                       const uint8_t* __restrict__ route,
                                                       const PeState* __restrict__ pe, int nb,
-                                                      int shift, unsigned long long* hist_cnt,
+                                                      int rows_per_cta, int shift,
+                                                      unsigned long long* hist_cnt,
                                                       double* hist_mass) {
   const int h = blockIdx.y;
   if (route[h]) return;
@@ -467,8 +471,8 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
       m0 = v;
     }
   };
-  const int I0 = blockIdx.x * kHistRows;
-  for (int I = I0; I < min(nb, I0 + kHistRows); ++I) {
+  const int I0 = blockIdx.x * rows_per_cta;
+  for (int I = I0; I < min(nb, I0 + rows_per_cta); ++I) {
     const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
     const int len = I + 1;
     if ((nb & 3) == 0) {
@@ -513,54 +517,94 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
   }
 }
 
-// Picks the digit whose bin crosses the remaining target; one thread per head.
+// Picks the digit whose bin crosses the remaining target.  One warp per head: lane l holds
+// bins 255-8l .. 248-8l (descending), the lanes' fp64 masses are prefix-summed by shuffles,
+// and the first lane whose bins cross the target supplies the digit (the walk from the top
+// bin down that the cumulative-coverage rule describes, with the sums grouped by lane).
 __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, float gamma,
                                 PeState* pe, unsigned long long* hist_cnt, double* hist_mass) {
   const int h = blockIdx.x;
-  if (route[h] == 0 && threadIdx.x == 0) {
+  if (route[h] == 0 && threadIdx.x < 32) {
+    const int lane = threadIdx.x;
     PeState st = pe[h];
     if (!st.select_all) {
       const int shift = 24 - 8 * pass;
       const double rem = static_cast<double>(gamma) - st.mass_above;
-      double cum = 0.0;
-      int chosen = -1, lowest = -1;
-      for (int bin = 255; bin >= 0; --bin) {
-        const unsigned long long c = hist_cnt[h * 256 + bin];
-        if (!c) continue;
-        const double m = hist_mass[h * 256 + bin];
-        if (cum + m >= rem) {
-          chosen = bin;
-          break;
-        }
-        cum += m;
-        lowest = bin;
+      unsigned long long c[8];
+      double m[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int bin = 255 - (lane * 8 + i);
+        c[i] = hist_cnt[h * 256 + bin];
+        m[i] = hist_mass[h * 256 + bin];
       }
-      if (chosen < 0) {
-        if (pass == 0 || lowest < 0) {
+      double local = 0.0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c[i]) local += m[i];
+      double incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      double cum = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) cum = 0.0;
+      int cand = -1, low = -1;
+      double cand_cum = 0.0, low_m = 0.0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (!c[i]) continue;
+        const int bin = 255 - (lane * 8 + i);
+        if (cand < 0) {
+          if (cum + m[i] >= rem) {
+            cand = bin;
+            cand_cum = cum;
+          } else {
+            cum += m[i];
+          }
+        }
+        low = bin;
+        low_m = m[i];
+      }
+      int chosen = -1;
+      double above = 0.0;
+      const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        chosen = __shfl_sync(0xffffffffu, cand, src);
+        above = __shfl_sync(0xffffffffu, cand_cum, src);
+      } else {
+        const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
+        const double total = __shfl_sync(0xffffffffu, incl, 31);
+        if (pass == 0 || any == 0) {
           st.select_all = 1;  // the whole triangle holds less than gamma
         } else {
-          chosen = lowest;
-          cum -= hist_mass[h * 256 + lowest];
+          const int src = 31 - __clz(any);
+          chosen = __shfl_sync(0xffffffffu, low, src);
+          above = total - __shfl_sync(0xffffffffu, low_m, src);
         }
       }
-      if (!st.select_all) {
-        st.mass_above += cum;
-        st.prefix |= static_cast<uint32_t>(chosen) << shift;
-        st.decided |= 255u << shift;
-        if (pass == 3) {
-          st.thresh = st.prefix;
-          st.count_eq = hist_cnt[h * 256 + chosen];
-          const double vt = static_cast<double>(__uint_as_float(st.thresh));
-          const double rem2 = static_cast<double>(gamma) - st.mass_above;
-          unsigned long long need = st.count_eq;
-          if (vt > 0.0) {
-            const double q = ceil(rem2 / vt);
-            need = q < 1.0 ? 1ull : static_cast<unsigned long long>(q);
+      if (lane == 0) {
+        if (!st.select_all) {
+          st.mass_above += above;
+          st.prefix |= static_cast<uint32_t>(chosen) << shift;
+          st.decided |= 255u << shift;
+          if (pass == 3) {
+            st.thresh = st.prefix;
+            st.count_eq = hist_cnt[h * 256 + chosen];
+            const double vt = static_cast<double>(__uint_as_float(st.thresh));
+            const double rem2 = static_cast<double>(gamma) - st.mass_above;
+            unsigned long long need = st.count_eq;
+            if (vt > 0.0) {
+              const double q = ceil(rem2 / vt);
+              need = q < 1.0 ? 1ull : static_cast<unsigned long long>(q);
+            }
+            st.need_eq = need < st.count_eq ? need : st.count_eq;
           }
-          st.need_eq = need < st.count_eq ? need : st.count_eq;
         }
+        pe[h] = st;
       }
-      pe[h] = st;
     }
   }
   __syncthreads();
@@ -718,8 +762,9 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
   pe_prob_kernel<<<dim3(s.H, pa.nt), kPeThreads, kPeSmem, st>>>(tmQs, tmKs, tmO, pa);
   pe_radix_init_kernel<<<s.H, 256, 0, st>>>(w.pe, w.hist_cnt, w.hist_mass);
   for (int pass = 0; pass < 4; ++pass) {
-    pe_hist_kernel<<<dim3((s.nb + kHistRows - 1) / kHistRows, s.H), 256, 0, st>>>(
-        w.pev, w.route, w.pe, s.nb, 24 - 8 * pass, w.hist_cnt, w.hist_mass);
+    const int rpc = hist_rows_per_cta(s.nb);
+    pe_hist_kernel<<<dim3((s.nb + rpc - 1) / rpc, s.H), 256, 0, st>>>(
+        w.pev, w.route, w.pe, s.nb, rpc, 24 - 8 * pass, w.hist_cnt, w.hist_mass);
     pe_digit_kernel<<<s.H, 256, 0, st>>>(w.route, pass, cfg.gamma, w.pe, w.hist_cnt,
                                          w.hist_mass);
   }
