@@ -411,7 +411,7 @@ def run_sweep(args):
     from workloads.configs import SWEEP
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
-    pts = []
+    pts, pts_g = [], []
     for name in SWEEP:
         w = get(name)
         g = make_inputs(w)
@@ -438,6 +438,10 @@ def run_sweep(args):
         reps = 10 if w.n <= 65536 else 3
         sel_ms = timed(lambda: ctx.select(dims, q, k, cfg), reps)
         pre_ms = timed(lambda: ctx.prefill(dims, q, k, v, cfg, o), reps)
+        # the same call replayed from a captured CUDA graph (the first call captures it)
+        gcfg = dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy,
+                               k_min_tokens=w.k_min_tokens, flags=dsp.FLAG_GRAPH_REPLAY)
+        pre_g_ms = timed(lambda: ctx.prefill(dims, q, k, v, gcfg, o), reps)
         att_ms = timed(lambda: ctx.attend(dims, q, k, v, o), reps)
         den_ms = timed(lambda: ctx.dense(dims, q, k, v, o), max(1, reps // 2))
         if ctx.sync_status() != 0:
@@ -445,27 +449,33 @@ def run_sweep(args):
         st = ctx.stats(dims)
         nbk = w.n // B
         line = {"sweep": True, "workload": name, "n": w.n, "prefill_ms": pre_ms,
+                "prefill_graph_ms": pre_g_ms,
                 "select_ms": sel_ms, "attend_ms": att_ms, "dense_ms": den_ms,
                 "speedup_vs_dense": den_ms / pre_ms,
+                "speedup_vs_dense_graph": den_ms / pre_g_ms,
                 "attend_tflops": algorithmic_flops(st["nnz"], st["rows"]) / (att_ms * 1e-3) / 1e12,
                 "dense_tflops": algorithmic_flops(w.hq * nbk * (nbk + 1) // 2, w.hq * nbk)
                 / (den_ms * 1e-3) / 1e12,
                 "density": st["nnz"] / (w.hq * nbk * (nbk + 1) / 2)}
         print(json.dumps(line), flush=True)
         pts.append((w.n, den_ms / pre_ms))
+        pts_g.append((w.n, den_ms / pre_g_ms))
         ctx.close()
         del q, k, v, o
         torch.cuda.empty_cache()
-    cross = None
-    for (n0, s0), (n1, s1) in zip(pts, pts[1:]):
-        if s0 < 1.0 <= s1:
-            f = (math.log(1.0) - math.log(s0)) / (math.log(s1) - math.log(s0))
-            cross = math.exp(math.log(n0) + f * (math.log(n1) - math.log(n0)))
-            break
-    if cross is None and pts and pts[0][1] >= 1.0:
-        cross = f"below {pts[0][0]}"
-    print(json.dumps({"sweep_summary": True, "crossover_tokens": cross,
-                      "speedups": {n: s for n, s in pts}}), flush=True)
+    def crossover(p):
+        for (n0, s0), (n1, s1) in zip(p, p[1:]):
+            if s0 < 1.0 <= s1:
+                f = (math.log(1.0) - math.log(s0)) / (math.log(s1) - math.log(s0))
+                return math.exp(math.log(n0) + f * (math.log(n1) - math.log(n0)))
+        if p and p[0][1] >= 1.0:
+            return f"below {p[0][0]}"
+        return None
+
+    print(json.dumps({"sweep_summary": True, "crossover_tokens": crossover(pts),
+                      "crossover_tokens_graph": crossover(pts_g),
+                      "speedups": {n: s for n, s in pts},
+                      "speedups_graph": {n: s for n, s in pts_g}}), flush=True)
 
 
 def run_jsd(args):

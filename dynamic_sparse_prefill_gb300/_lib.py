@@ -20,6 +20,7 @@ FLAG_FORCE_VS = 0x1
 FLAG_FORCE_PE = 0x2
 FLAG_MEDIAN_FLOOR = 0x4
 FLAG_VS_GAMMA_CUMSUM = 0x8
+FLAG_GRAPH_REPLAY = 0x10
 DEBUG_DROP_ARRIVE = 0x1
 
 # Every entry point include/crisp.h declares.

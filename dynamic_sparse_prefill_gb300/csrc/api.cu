@@ -143,6 +143,7 @@ bool create_copy_streams(crisp_ctx ctx) {
   const unsigned f = cudaEventDisableTiming;
   if (cudaStreamCreateWithFlags(&ctx->h2d, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&ctx->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ctx->cap, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&ctx->ev_entry, f) != cudaSuccess ||
       cudaEventCreateWithFlags(&ctx->ev_done, f) != cudaSuccess)
     return false;
@@ -162,6 +163,8 @@ void destroy_copy_streams(crisp_ctx ctx) {
   if (ctx->ev_done) cudaEventDestroy(ctx->ev_done);
   if (ctx->h2d) cudaStreamDestroy(ctx->h2d);
   if (ctx->d2h) cudaStreamDestroy(ctx->d2h);
+  if (ctx->graph_exec) cudaGraphExecDestroy(ctx->graph_exec);
+  if (ctx->cap) cudaStreamDestroy(ctx->cap);
   cudaGetLastError();
 }
 
@@ -398,9 +401,78 @@ crisp_status crisp_dense(crisp_ctx ctx, const crisp_dims* dims, const void* Q, c
   return run_attention(ctx, dims, Q, K, V, O, true, stream);
 }
 
+// crisp_prefill with CRISP_FLAG_GRAPH_REPLAY: capture select + attend on the context's own
+// stream (the caller's may be the legacy default stream, which cannot be captured), keep
+// the executable graph, and launch it on the caller's stream.
+static crisp_status prefill_replay(crisp_ctx ctx, const crisp_dims* dims, const void* Q,
+                                   const void* K, const void* V, const crisp_cfg* cfg, void* O,
+                                   void* stream) {
+  crisp_status st = check_common(ctx, dims);
+  if (st != CRISP_OK) return st;
+  if ((st = check_cfg(cfg)) != CRISP_OK) return st;
+  GraphKey key;
+  memset(&key, 0, sizeof(key));
+  key.dims = *dims;
+  key.cfg = *cfg;
+  key.q = Q;
+  key.k = K;
+  key.v = V;
+  key.o = O;
+  key.timeout_ns = ctx->timeout_ns;
+  key.debug_flags = ctx->debug_flags;
+  if (!ctx->graph_exec || memcmp(&key, &ctx->graph_key, sizeof(key)) != 0) {
+    if (ctx->graph_exec) {
+      cudaGraphExecDestroy(ctx->graph_exec);
+      ctx->graph_exec = nullptr;
+    }
+    crisp_cfg eager = *cfg;
+    eager.flags &= ~CRISP_FLAG_GRAPH_REPLAY;
+    cudaError_t e = cudaStreamBeginCapture(ctx->cap, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+      set_err(ctx, "cudaStreamBeginCapture", e);
+      return CRISP_ERR_CUDA;
+    }
+    st = crisp_select(ctx, dims, Q, K, &eager, ctx->cap);
+    if (st == CRISP_OK) st = crisp_attend(ctx, dims, Q, K, V, O, ctx->cap);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(ctx->cap, &g);
+    if (st == CRISP_OK && (e != cudaSuccess || !g)) {
+      set_err(ctx, "cudaStreamEndCapture", e);
+      st = CRISP_ERR_CUDA;
+    }
+    if (st == CRISP_OK) {
+      e = cudaGraphInstantiate(&ctx->graph_exec, g, 0);
+      if (e != cudaSuccess) {
+        ctx->graph_exec = nullptr;
+        set_err(ctx, "cudaGraphInstantiate", e);
+        st = CRISP_ERR_CUDA;
+      }
+    }
+    if (g) cudaGraphDestroy(g);
+    if (st != CRISP_OK) {
+      cudaGetLastError();
+      ctx->has_sel = false;
+      ctx->has_patsearch = false;
+      return st;
+    }
+    ctx->graph_key = key;
+  }
+  const cudaError_t e = cudaGraphLaunch(ctx->graph_exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_err(ctx, "cudaGraphLaunch", e);
+    return CRISP_ERR_CUDA;
+  }
+  ctx->has_sel = true;
+  ctx->has_patsearch = true;
+  ctx->sel_dims = *dims;
+  return CRISP_OK;
+}
+
 crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q, const void* K,
                            const void* V, const crisp_cfg* cfg, void* O, void* stream) {
   if (!V || !O) return CRISP_ERR_INVALID_ARG;
+  if (cfg && (cfg->flags & CRISP_FLAG_GRAPH_REPLAY))
+    return prefill_replay(ctx, dims, Q, K, V, cfg, O, stream);
   crisp_status st = crisp_select(ctx, dims, Q, K, cfg, stream);
   if (st != CRISP_OK) return st;
   return crisp_attend(ctx, dims, Q, K, V, O, stream);

@@ -78,6 +78,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// What a captured crisp_prefill graph depends on (compared bytewise; zero-filled first).
+struct GraphKey {
+  crisp_dims dims;
+  crisp_cfg cfg;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  uint64_t timeout_ns;
+  uint32_t debug_flags;
+};
+
 // Shapes of one call, flattened: H = batch*hq query heads, Hkv = batch*hkv.
 struct Shape {
   int n, nb, nbw, H, Hkv, hq, hkv, group;
@@ -103,6 +115,10 @@ struct crisp_ctx_s {
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t ev_entry = nullptr, ev_done = nullptr;
   cudaEvent_t ev_in[kMaxChunks] = {}, ev_out[kMaxChunks] = {};
+  // crisp_prefill with CRISP_FLAG_GRAPH_REPLAY: capture stream and the last call's graph.
+  cudaStream_t cap = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  crisp::GraphKey graph_key{};
   char last_err[256] = {0};
 };
 

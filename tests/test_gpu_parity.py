@@ -142,6 +142,48 @@ def test_edge_shapes_clipped_prob_stores(dsp, n, hq, hkv, seed):
         run_parity(dsp, w, g, sample=(hq, 6), seed=seed, flags=flags)
 
 
+def test_prefill_graph_replay_matches_eager(dsp):
+    """CRISP_FLAG_GRAPH_REPLAY: the captured graph reproduces the eager crisp_prefill bit for
+    bit (output and selection), repeated calls replay it, and a new output pointer or a new
+    cfg is captured again."""
+    w = get("llama8b_n32k")
+    g = generate(w, q_heads=range(8), kv_heads=range(2))
+    w = w.with_params(hq=8, hkv=2)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+
+    def run(wl, flags, o):
+        ctx.prefill(dims, q, k, v, _cfg(dsp, wl, flags=flags), o)
+        torch.cuda.synchronize()
+        assert ctx.sync_status() == 0
+        return ctx.selection_get(dims)
+
+    def same_sel(a, b):
+        assert a.keys() == b.keys()
+        for key in a:
+            assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+
+    o_e = torch.empty_like(q)
+    sel_e = run(w, 0, o_e)
+    o_g = torch.full_like(q, 7.0)
+    for _ in range(3):  # capture, then two replays
+        sel_g = run(w, dsp.FLAG_GRAPH_REPLAY, o_g)
+        assert torch.equal(o_e, o_g)
+        same_sel(sel_e, sel_g)
+    o_g2 = torch.zeros_like(q)
+    run(w, dsp.FLAG_GRAPH_REPLAY, o_g2)
+    assert torch.equal(o_e, o_g2)
+    w2 = w.with_params(alpha=2.0, gamma=0.9)
+    o_e2, o_g3 = torch.empty_like(q), torch.zeros_like(q)
+    sel_e2 = run(w2, 0, o_e2)
+    sel_g3 = run(w2, dsp.FLAG_GRAPH_REPLAY, o_g3)
+    assert torch.equal(o_e2, o_g3)
+    same_sel(sel_e2, sel_g3)
+    assert not torch.equal(o_e, o_e2)
+    ctx.close()
+
+
 @pytest.mark.parametrize("alpha,kmin,gamma", [(0.0, 0, 0.5), (1.25, 0, 0.95), (1.0, 4096, 1.0),
                                               (3.0, 256, 0.99)])
 def test_parameter_edges(dsp, alpha, kmin, gamma):
