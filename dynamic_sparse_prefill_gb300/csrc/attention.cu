@@ -166,8 +166,8 @@ struct Item {
 };
 
 // Item at position ke of the launch's order: a listed row (rescue pass), a row of the
-// sparse order, or the dense enumeration (KV head major, query block descending, the
-// group's q-heads adjacent).
+// sparse order, or the dense enumeration (within a launch's KV heads: query block
+// descending, then KV head, the group's q-heads adjacent).
 __device__ __forceinline__ Item item_of(const AttnArgs& a, int ke) {
   Item it;
   if (a.list != nullptr) {
@@ -175,9 +175,11 @@ __device__ __forceinline__ Item item_of(const AttnArgs& a, int ke) {
     it.h = row / a.nb;
     it.I = row % a.nb;
   } else if (a.dense) {
-    const int per_kv = a.group * a.nb;
-    const int hk_all = ke / per_kv, r = ke % per_kv;
-    it.I = a.nb - 1 - r / a.group;
+    const int per_I = a.num_items / a.nb;  // rows per query block in this launch
+    const int local = ke - a.item_base;
+    const int r = local % per_I;
+    const int hk_all = a.item_base / (a.group * a.nb) + r / a.group;
+    it.I = a.nb - 1 - local / per_I;
     it.h = (hk_all / a.hkv) * a.hq + (hk_all % a.hkv) * a.group + r % a.group;
   } else {
     const int row = a.order[ke];
@@ -1004,21 +1006,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Counting sort of the selection's rows by (KV head, descending length): the attention
-// kernel walks this order in serpentine waves (see get_item).  Rows with the same key keep
-// no particular order.
+// Counting sort of the selection's rows by (launch, descending length), a launch being
+// `per` consecutive KV heads: each launch of the fast kernel hands its rows out longest
+// first across all of its KV heads.  Rows with the same key keep no particular order.
 __device__ __forceinline__ int order_key(const int64_t* row_ptr, int row, int nb, int hq, int hkv,
-                                         int group) {
+                                         int group, int per) {
   const int h = row / nb;
   const int hk = (h / hq) * hkv + (h % hq) / group;
   const int len = static_cast<int>(row_ptr[row + 1] - row_ptr[row]);
-  return hk * (nb + 1) + (nb - len);
+  return (hk / per) * (nb + 1) + (nb - len);
 }
 
 __global__ void order_hist_kernel(const int64_t* __restrict__ row_ptr, int rows, int nb, int hq,
-                                  int hkv, int group, int* hist) {
+                                  int hkv, int group, int per, int* hist) {
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row < rows) atomicAdd(&hist[order_key(row_ptr, row, nb, hq, hkv, group)], 1);
+  if (row < rows) atomicAdd(&hist[order_key(row_ptr, row, nb, hq, hkv, group, per)], 1);
 }
 
 // In-place exclusive scan of nbins counts (one CTA).
@@ -1045,16 +1047,23 @@ __global__ void __launch_bounds__(1024) order_scan_kernel(int* hist, int nbins) 
 }
 
 __global__ void order_scatter_kernel(const int64_t* __restrict__ row_ptr, int rows, int nb, int hq,
-                                     int hkv, int group, int* cursor, int32_t* order) {
+                                     int hkv, int group, int per, int* cursor, int32_t* order) {
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row < rows) order[atomicAdd(&cursor[order_key(row_ptr, row, nb, hq, hkv, group)], 1)] = row;
+  if (row < rows)
+    order[atomicAdd(&cursor[order_key(row_ptr, row, nb, hq, hkv, group, per)], 1)] = row;
 }
 
 }  // namespace
 
+// KV heads per launch of the fast kernel: enough rows for 8 per SM, and beyond that as many
+// KV heads as keep their K and V (2 x n x 128 x 2 bytes each) within 48 MB of L2, so that
+// short sequences run in few launches (each launch pays a start and a tail).
 int attention_kv_heads_per_launch(const Shape& s, int num_sms) {
   const int per_kv = s.group * s.nb;
-  const int per = (8 * num_sms + per_kv - 1) / per_kv;
+  int per = (8 * num_sms + per_kv - 1) / per_kv;
+  const int64_t kv_bytes = 2ll * s.n * kD * 2;
+  const int l2_fit = static_cast<int>((48ll << 20) / kv_bytes);
+  per = per > l2_fit ? per : l2_fit;
   return per < 1 ? 1 : (per > s.Hkv ? s.Hkv : per);
 }
 
@@ -1074,16 +1083,23 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.col = ctx->ws.col;
   a.order = ctx->ws.order;
   a.dense = dense ? 1 : 0;
+  // One launch per group of `per` KV heads (every KV head owns group * N_b rows): all CTAs
+  // of a launch then stream the same few KV heads' blocks, which keeps them in L2 (at 512k
+  // tokens, 3x less DRAM traffic than one launch over every head).
+  const int per_kv = s.group * s.nb;
+  const int per = attention_kv_heads_per_launch(s, ctx->num_sms);
+  const int nlaunch = (s.Hkv + per - 1) / per;
   if (!dense) {
     const int rows = s.H * s.nb;
-    const int nbins = s.Hkv * (s.nb + 1);
+    const int nbins = nlaunch * (s.nb + 1);
     cudaError_t e = cudaMemsetAsync(ctx->ws.len_hist, 0, sizeof(int) * nbins, st);
     if (e != cudaSuccess) return e;
     order_hist_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows, s.nb, s.hq, s.hkv,
-                                                          s.group, ctx->ws.len_hist);
+                                                          s.group, per, ctx->ws.len_hist);
     order_scan_kernel<<<1, 1024, 0, st>>>(ctx->ws.len_hist, nbins);
-    order_scatter_kernel<<<(rows + 255) / 256, 256, 0, st>>>(
-        ctx->ws.row_ptr, rows, s.nb, s.hq, s.hkv, s.group, ctx->ws.len_hist, ctx->ws.order);
+    order_scatter_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows, s.nb, s.hq,
+                                                             s.hkv, s.group, per,
+                                                             ctx->ws.len_hist, ctx->ws.order);
   }
   a.O = static_cast<uint16_t*>(O);
   a.err = ctx->ws.err;
@@ -1095,13 +1111,6 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.redo_count = ctx->ws.redo_count;
   cudaError_t e = cudaMemsetAsync(ctx->ws.redo_count, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
-  // One launch per group of KV heads (the order is KV-head major and every KV head owns
-  // group * N_b rows): all CTAs of a launch then stream the same KV head's blocks, which
-  // keeps them in L2 (at 512k tokens, 3x less DRAM traffic than one launch over every
-  // head).  A group holds enough rows for 8 per SM.
-  const int per_kv = s.group * s.nb;
-  const int per = attention_kv_heads_per_launch(s, ctx->num_sms);
-  const int nlaunch = (s.Hkv + per - 1) / per;
   e = cudaMemsetAsync(ctx->ws.work_ctr, 0, sizeof(int) * nlaunch, st);
   if (e != cudaSuccess) return e;
   for (int g0 = 0; g0 < s.Hkv; g0 += per) {
