@@ -446,6 +446,17 @@ def test_llama_n512k_sampled_and_dense(dsp):
     ctx.close()
 
 
+def test_max_length_n1m(dsp):
+    """The longest supported sequence (n = 2^20, N_b = 8192: the VS selection's shared-memory
+    sort at its size limit, an 8192 x 8192 PE triangle), one VS-planted and one PE head:
+    full selection parity, outputs on sampled query blocks."""
+    w = Workload("max_n1m", n=1 << 20, hq=2, hkv=1, seed=2024, sink_scale=4.0,
+                 needles=("fixed", 6), pe_heads=(1,))
+    rep, sel, _ = run_parity(dsp, w, generate(w), sample=(2, 3), seed=5)
+    assert rep["vs_heads"] + rep["pe_heads"] == 2
+    print("max_n1m", rep)
+
+
 @pytest.mark.parametrize("name,sample", [("llama8b_n8k", None), ("llama8b_n16k", None),
                                          ("llama8b_n64k", (8, 16)), ("llama8b_n256k", (8, 16))])
 def test_sweep_lengths(dsp, name, sample):
