@@ -35,14 +35,10 @@ UNIT = "ms/layer"
 B = 128
 D = 128
 def launches_per_prefill(w, sms: int) -> int:
-    """Kernel launches of one crisp_prefill: PatSearch 4, PEIndex 16, CSR 4, work order 3,
-    then the fast attention kernel once per group of KV heads (each group holds at least 8
-    query-block rows per SM, the library's rule) and the rescue pass once (it returns at
-    once when no row was listed)."""
-    per_kv = (w.hq // w.hkv) * (w.n // B)
-    hkv = w.batch * w.hkv
-    per = min(max(-(-8 * sms // per_kv), 1), hkv)
-    return 27 + -(-hkv // per) + 1
+    """Kernel launches of one crisp_prefill, as the library plans them (selection, work
+    order, the fast attention kernel once per group of KV heads, the rescue pass)."""
+    import dynamic_sparse_prefill_gb300 as dsp
+    return dsp.prefill_launches(dsp.make_dims(w.batch, w.n, w.hq, w.hkv), sms)
 
 
 def algorithmic_flops(nnz: int, rows: int) -> float:

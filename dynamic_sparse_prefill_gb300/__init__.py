@@ -8,7 +8,7 @@ the library and fails if it has not been built; there is no fallback path.
 from ._lib import (  # noqa: F401
     DEBUG_DROP_ARRIVE, FLAG_FORCE_PE, FLAG_FORCE_VS, FLAG_GRAPH_REPLAY, FLAG_MEDIAN_FLOOR,
     FLAG_VS_GAMMA_CUMSUM, Cfg, Context, CrispError, Dims, LIB_PATH,
-    default_cfg, lib, make_dims,
+    default_cfg, lib, make_dims, prefill_launches,
 )
 
 lib()

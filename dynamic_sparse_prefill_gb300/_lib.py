@@ -28,7 +28,7 @@ EXPORTED = ["crisp_cfg_default", "crisp_create", "crisp_destroy", "crisp_select"
             "crisp_prefill", "crisp_dense", "crisp_selection_get", "crisp_selection_set",
             "crisp_selection_stats", "crisp_sync_status", "crisp_set_debug",
             "crisp_status_string", "crisp_last_error", "crisp_route_static", "crisp_jsd",
-            "crisp_attend_info", "crisp_prefill_host"]
+            "crisp_attend_info", "crisp_prefill_host", "crisp_prefill_launches"]
 
 
 class Dims(ctypes.Structure):
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "crisp_last_error": (ctypes.c_char_p, [P]),
         "crisp_route_static": (ctypes.c_int, [DP, P, P, CP, P, P, P, P]),
         "crisp_jsd": (ctypes.c_int, [P, DP, P, P, ctypes.c_float, P, P, P]),
+        "crisp_prefill_launches": (ctypes.c_int32, [DP, ctypes.c_int32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -126,6 +127,11 @@ def default_cfg(**kw) -> Cfg:
 
 def make_dims(batch, n, hq, hkv, d=128) -> Dims:
     return Dims(batch, n, hq, hkv, d)
+
+
+def prefill_launches(dims: Dims, num_sms: int) -> int:
+    """Kernel launches of one crisp_prefill on a GPU with num_sms SMs (host arithmetic)."""
+    return int(lib().crisp_prefill_launches(ctypes.byref(dims), num_sms))
 
 
 class Context:

@@ -478,6 +478,13 @@ crisp_status crisp_prefill(crisp_ctx ctx, const crisp_dims* dims, const void* Q,
   return crisp_attend(ctx, dims, Q, K, V, O, stream);
 }
 
+int32_t crisp_prefill_launches(const crisp_dims* dims, int32_t num_sms) {
+  if (!dims || num_sms < 1 || check_dims(dims) != CRISP_OK) return 0;
+  const Shape s = make_shape(*dims);
+  const int per = attention_kv_heads_per_launch(s, num_sms);
+  return 23 + 3 + (s.Hkv + per - 1) / per + 1;
+}
+
 crisp_status crisp_prefill_host(crisp_ctx ctx, const crisp_dims* dims, const void* Q_host,
                                 const void* K_host, const void* V_host, const crisp_cfg* cfg,
                                 void* O_host, void* Q, void* K, void* V, void* O, void* stream) {

@@ -211,6 +211,12 @@ crisp_status crisp_jsd(crisp_ctx ctx, const crisp_dims* dims, const void* Q, con
  * maxima ("Prerequisites": exact softmax attention either way).  Normally 0. */
 crisp_status crisp_attend_info(crisp_ctx ctx, void* stream, int64_t* rows);
 
+/* Number of kernel launches one crisp_prefill enqueues for `dims` on a GPU with `num_sms`
+ * SMs: selection 23 (PatSearch 4, PEIndex 15, CSR 4), the attention work order 3, the
+ * fast attention kernel once per group of KV heads, and the rescue pass once.  Host-only
+ * arithmetic (no context, no CUDA call); 0 for dims the library does not support. */
+int32_t crisp_prefill_launches(const crisp_dims* dims, int32_t num_sms);
+
 /* Synchronise `stream`, then report and clear the device error word: CRISP_OK,
  * CRISP_ERR_TIMEOUT or CRISP_ERR_DEVICE_ASSERT, or CRISP_ERR_CUDA if the stream itself
  * reports a CUDA error. */

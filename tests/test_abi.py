@@ -31,6 +31,23 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(lib, name), name
 
 
+def test_prefill_launch_plan(L):
+    """Launches per crisp_prefill on 152 SMs: 23 selection + 3 work order + the attention
+    launches (KV heads per launch: >= 8 rows per SM, or as many as fit 48 MB of L2) + 1."""
+    lib = L.lib()
+    cases = [((1, 524288, 32, 8), 26 + 8 + 1),    # one KV head per launch
+             ((1, 131072, 32, 8), 26 + 8 + 1),
+             ((1, 32768, 32, 8), 26 + 3 + 1),     # 16 MiB of K+V per KV head: 3 per launch
+             ((1, 8192, 32, 8), 26 + 1 + 1),      # everything in one launch
+             ((1, 4096, 2, 2), 26 + 1 + 1),
+             ((2, 16384, 32, 8), 26 + 3 + 1)]     # 16 KV heads, 6 per launch (8 MiB each)
+    for (b, n, hq, hkv), want in cases:
+        d = L.make_dims(b, n, hq, hkv)
+        assert lib.crisp_prefill_launches(ctypes.byref(d), 152) == want, (b, n, hq, hkv)
+    assert lib.crisp_prefill_launches(ctypes.byref(L.make_dims(1, 100, 2, 2)), 152) == 0
+    assert lib.crisp_prefill_launches(ctypes.byref(L.make_dims(1, 4096, 2, 2)), 0) == 0
+
+
 def test_default_cfg_is_the_pages_defaults(L):
     c = L.lib().crisp_cfg_default()
     assert (c.B, c.b, c.w_sink, c.w_local, c.k_min_tokens) == (128, 128, 128, 128, 1024)
