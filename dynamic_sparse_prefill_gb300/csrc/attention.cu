@@ -8,7 +8,8 @@
 // block K <= I selected this is dense causal attention, the speedup denominator.
 //
 // Two persistent kernels, one CTA per SM, over work items (query head h, query block I)
-// in an order that keeps each KV head's rows together, longest first.  The fast kernel
+// in an order that keeps each launch's KV heads together, longest row first across them
+// (one KV head per launch at long lengths, a few at short ones).  The fast kernel
 // hands items out dynamically (a per-launch counter and a shared-memory item ring, see
 // ItemFeed); the rescue kernel walks its short list in static serpentine waves (see
 // get_item).  Both use the same warp roles:
