@@ -284,6 +284,48 @@ def test_rescue_pass_recomputes_overflowing_rows(dsp):
     ctx.close()
 
 
+@pytest.mark.parametrize("n,hq,hkv,seed", [(4096, 4, 2, 71), (4736, 4, 1, 72)])
+def test_attend_random_index_sets(dsp, n, hq, hkv, seed):
+    """crisp_attend on arbitrary caller-supplied index sets (crisp_selection_set): per row a
+    random non-empty subset of [0, I] whose density ranges from one block to every block,
+    the diagonal block included or not, N_b = 32 and a ragged 37; every query block of
+    every head against the oracle's exact attention on the same sets."""
+    from oracle import crisp_oracle as O
+    nb = n // 128
+    g = random_qkv(n, hq, hkv, 128, seed, scale=3.0)
+    rng = np.random.default_rng(seed)
+    masks = []
+    for h in range(hq):
+        m = np.zeros((nb, nb), bool)
+        for I in range(nb):
+            p = rng.choice([0.0, 0.15, 0.5, 1.0])
+            row = rng.random(I + 1) < p
+            if rng.random() < 0.7:
+                row[I] = True
+            if not row.any():
+                row[rng.integers(0, I + 1)] = True
+            m[I, : I + 1] = row
+        masks.append(m)
+    assert any(not masks[h][I, I] for h in range(hq) for I in range(1, nb))
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    dims = dsp.make_dims(1, n, hq, hkv)
+    ctx = dsp.Context(dims)
+    rp, col = csr_from_masks(masks, nb)
+    ctx.selection_set(dims, rp, col)
+    o = torch.empty_like(q)
+    ctx.attend(dims, q, k, v, o)
+    assert ctx.sync_status() == 0
+    got = o.float().cpu().numpy()
+    grp = hq // hkv
+    for h in range(hq):
+        ref = O.block_sparse_attention(O.bf16_bits_to_f64(g["q"][h]),
+                                       O.bf16_bits_to_f64(g["k"][h // grp]),
+                                       O.bf16_bits_to_f64(g["v"][h // grp]), masks[h], 128,
+                                       list(range(nb)))
+        compare_outputs(got[h], ref, f"random index sets, head {h}")
+    ctx.close()
+
+
 @pytest.mark.parametrize("name", ["tiny_n4k", "llama8b_n32k"])
 def test_prefill_host_matches_device_path(dsp, name):
     """crisp_prefill_host (host buffers, chunked by KV-head groups, copies overlapped)
