@@ -613,33 +613,37 @@ __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, flo
   hist_mass[h * 256 + threadIdx.x] = 0.0;
 }
 
-// Number of items equal to the threshold in each PE row (for flat-order tie ranks).
+// Number of items equal to the threshold in each PE row (for flat-order tie ranks): a warp
+// per row, four coalesced loads in flight per lane.
 __global__ void __launch_bounds__(256) pe_eqcount_kernel(const float* __restrict__ pev,
                                                          const uint8_t* __restrict__ route,
                                                          const PeState* __restrict__ pe,
                                                          int nb, int64_t* eq_off) {
-  const int h = blockIdx.y, I = blockIdx.x;
+  const int h = blockIdx.y;
   if (route[h]) return;
   const PeState st = pe[h];
   if (st.select_all || st.need_eq >= st.count_eq) return;  // no tie ranks needed
-  __shared__ int red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int I = blockIdx.x * 8 + warp;
+  if (I >= nb) return;
+  const uint32_t* row =
+      reinterpret_cast<const uint32_t*>(pev + (static_cast<size_t>(h) * nb + I) * nb);
   int c = 0;
-  {
-    const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
-    for (int K = threadIdx.x; K <= I; K += 256) c += __float_as_uint(row[K]) == st.thresh;
+  for (int K0 = 0; K0 <= I; K0 += 128) {
+    uint32_t x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int K = K0 + u * 32 + lane;
+      x[u] = K <= I ? row[K] : ~st.thresh;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) c += x[u] == st.thresh ? 1 : 0;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int t = 0;
-    for (int i = 0; i < 8; ++i) t += red[i];
-    eq_off[static_cast<size_t>(h) * (nb + 1) + I] = t;
-  }
+  if (lane == 0) eq_off[static_cast<size_t>(h) * (nb + 1) + I] = c;
 }
 
-// In-place exclusive scan of the per-row counts of one head (nb <= 8192 entries).
 __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restrict__ route,
                                                          const PeState* __restrict__ pe, int nb,
                                                          int64_t* eq_off) {
@@ -769,7 +773,8 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
     pe_digit_kernel<<<s.H, 256, 0, st>>>(w.route, pass, cfg.gamma, w.pe, w.hist_cnt,
                                          w.hist_mass);
   }
-  pe_eqcount_kernel<<<dim3(s.nb, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, s.nb, w.eq_off);
+  pe_eqcount_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, s.nb,
+                                                                w.eq_off);
   pe_eqscan_kernel<<<s.H, 1024, 0, st>>>(w.route, w.pe, s.nb, w.eq_off);
   pe_mask_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, w.eq_off, s.nb,
                                                             s.nbw, w.rowmask, w.counts);

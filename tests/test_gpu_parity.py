@@ -7,8 +7,8 @@ the oracle's own index set must be within max abs 2e-2 / mean abs 2e-3 (tests/pa
 import numpy as np
 import pytest
 
-from tests.parity import (compare_outputs, compare_selection, csr_from_masks, oracle_outputs,
-                          oracle_select, to_device)
+from tests.parity import (compare_outputs, compare_selection, csr_from_masks, gpu_masks,
+                          oracle_outputs, oracle_select, to_device)
 from workloads import get
 from workloads.configs import Workload
 from workloads.planted import generate, random_qkv
@@ -282,6 +282,32 @@ def test_rescue_pass_recomputes_overflowing_rows(dsp):
             ref = O.block_sparse_attention(qf[h], kf, vf, np.tril(masks[h]), 128, list(range(nb)))
             compare_outputs(got[h], ref, f"sparse with_key={with_key}, head {h}")
     ctx.close()
+
+
+def test_pe_tie_ranks_exact_on_zero_queries(dsp):
+    """Queries of zeros make every pooled score 0, so row I of the PE triangle holds I + 1
+    equal values v = 1/((I+1) N_b): each row carries 1/N_b of the mass and ties decide the
+    cut.  With N_b = 32 and gamma = 0.95, rows 0..29 are taken whole and the remaining
+    0.0125 comes from row 30's first ceil(0.0125 * 32 * 31) = 13 keys in flat order (tie
+    ranks across the head), plus the forced diagonals (row 30's, row 31's).  The GPU's
+    index set must equal the oracle's and this closed form exactly (no exemption)."""
+    n, hq, hkv = 4096, 2, 1
+    nb = n // 128
+    g = random_qkv(n, hq, hkv, 128, seed=81, scale=3.0)
+    g["q"][:] = 0
+    w = Workload("zero_q", n=n, hq=hq, hkv=hkv, seed=81)
+    rep, sel, osel = run_parity(dsp, w, g, flags=dsp.FLAG_FORCE_PE)
+    expect = np.tril(np.ones((nb, nb), bool))
+    expect[30] = False
+    expect[30, :13] = True
+    expect[30, 30] = True
+    expect[31] = False
+    expect[31, 31] = True
+    gm = gpu_masks(sel, hq, nb)
+    for h in range(hq):
+        assert np.array_equal(np.tril(osel[h]["mask"]), expect), h
+        assert np.array_equal(gm[h], expect), h
+    assert rep["pe_pair_exempt"] == 0
 
 
 @pytest.mark.parametrize("n,hq,hkv,seed", [(4096, 4, 2, 71), (4736, 4, 1, 72)])
