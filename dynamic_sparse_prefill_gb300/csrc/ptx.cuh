@@ -1,6 +1,7 @@
 // ptx.cuh -- hand-written inline PTX for sm_103a: mbarriers with bounded waits, TMA tile
-// loads, and the tcgen05 tensor-core path (TMEM allocation, MMA, commit, TMEM loads and
-// stores), plus the shared-memory and instruction descriptors the MMAs take.
+// loads and stores (bulk async-group completion for the stores), and the tcgen05
+// tensor-core path (TMEM allocation, MMA, commit, TMEM loads and stores), plus the
+// shared-memory and instruction descriptors the MMAs take.
 //
 // Operand layout used throughout: a 128-row bf16 tile with 128 columns is stored as two
 // "regions" of 128 rows x 64 columns (128 bytes per row), written by TMA with 128-byte
