@@ -14,8 +14,11 @@ below name that page's sections:
   [Alg2] [Alg3] [Alg4]  the descriptions of Algorithms 2 (PatSearch), 3 (VSIndex) and
              4 (PEIndex) under "Figures and tables"
 
-Everything is computed in float64 from the exact bf16 inputs.  Readings of points the
-page leaves open are marked "Reading:"; they are the ones listed in the design notes.
+Everything is computed in float64 from the exact bf16 inputs.  Where the page leaves a
+point open (the "Method step details" prose and the Algorithm 3 and 4 descriptions name
+an operation without fixing its normalisation, direction or tie order), the plainest
+reading consistent with the rest of the page is taken and marked "Reading:" beside the
+step it affects.
 
 Every function here is pinned by tests in tests/test_oracle_pins.py against closed
 forms, special cases, brute force or a worked example; none is "parity unpinned".

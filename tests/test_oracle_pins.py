@@ -388,3 +388,85 @@ def test_pooled_estimate_special_cases():
     z = kb @ kb[3] / math.sqrt(d)
     ref = np.exp(z - z.max()) / np.exp(z - z.max()).sum()
     np.testing.assert_allclose(O.pooled_estimate(q, kc, B, b), ref, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- worked examples (PE, JSD)
+def _pe_worked_inputs(fx):
+    """Block-structured Q and K of the PE worked example: the key block means are e_K and
+    the query block means a_I with a_I[K] = 2 ln w[I][K] (K <= I), 2 ln 1000 (K > I); rows
+    inside a block differ by +-0.5 / +-0.25 along another axis, so only a block *mean*
+    gives those vectors."""
+    nb, B, d = len(fx["w"]), fx["B"], fx["d"]
+    c = np.array([0.5, -0.5, 0.25, -0.25])
+    assert B == c.size and d == nb
+    k = np.zeros((nb * B, d))
+    q = np.zeros((nb * B, d))
+    for blk in range(nb):
+        a = np.full(d, 2 * math.log(1000.0))
+        a[: blk + 1] = [2 * math.log(x) for x in fx["w"][blk]]
+        for r in range(B):
+            k[blk * B + r, blk] = 1.0
+            k[blk * B + r, (blk + 1) % d] += c[r]
+            q[blk * B + r] = a
+            q[blk * B + r, (blk + 2) % d] += c[r]
+    return q, k
+
+
+def test_pe_index_worked_example():
+    """PEIndex ("Method step details" step 3; Algorithm 4) on a case worked by hand in
+    tests/golden/pe_index_worked.json: block-mean pooling, the 1/sqrt(d) scale, the causal
+    block softmax, v = A_bar / N_b, the gamma-cumsum cut with flat-index ties, and the
+    diagonal rescue of an emptied row."""
+    from fractions import Fraction
+    fx = json.load(open(os.path.join(GOLD, "pe_index_worked.json")))
+    q, k = _pe_worked_inputs(fx)
+    nb = len(fx["w"])
+    # closed form of A_bar from the weights (exact fractions), and the fixture's copy
+    exact = np.zeros((nb, nb))
+    for I, row in enumerate(fx["w"]):
+        for K, x in enumerate(row):
+            exact[I, K] = float(Fraction(x, sum(row)))
+    np.testing.assert_array_equal(exact, np.array(fx["a_bar"], dtype=float))
+    for case in fx["cases"]:
+        pe = O.pe_index(q, k, fx["B"], case["gamma"])
+        np.testing.assert_allclose(pe["a_bar"], exact, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(pe["v"], exact / nb, rtol=0, atol=1e-13)
+        rows = [np.nonzero(pe["mask"][I])[0].tolist() for I in range(nb)]
+        assert rows == case["rows"], case["gamma"]
+        assert pe["n_selected"] == case["n_selected"]
+        assert abs(pe["v_star"] - case["v_star"]) < 1e-13
+        assert pe["rescued_rows"].tolist() == case["rescued_rows"]
+
+
+def test_jsd_route_worked_example():
+    """FlexPrefill's JSD routing ("Prerequisites", JSD) on a two-block case worked by hand
+    in tests/golden/jsd_route_worked.json: a_hat is the causal proxy attention averaged over
+    its rows and pooled by key block (the vertical score, not the slash score), a_bar the
+    softmax of the mean proxy query against the key block means, D_JS in nats."""
+    from fractions import Fraction
+    fx = json.load(open(os.path.join(GOLD, "jsd_route_worked.json")))
+    n, B, b, d = fx["n"], fx["B"], fx["b"], fx["d"]
+    w = fx["w_proxy"]
+    k = np.zeros((n, d))
+    k[:B, 0] = 1.0
+    k[B:, 1] = 1.0
+    q = np.zeros((n, d))
+    q[: n - b, 0] = 2 * math.log(50.0)
+    for r in range(b):
+        q[n - b + r, 0] = 2 * math.log(w[r])
+    # closed forms: Z_r = 4 w_r + r + 1; a_hat[0] = sum_r w_r / Z_r; a_bar from 72^(1/4)
+    a_hat0 = sum(Fraction(wr, 4 * wr + r + 1) for r, wr in enumerate(w))
+    a_hat = np.array([float(a_hat0), float(1 - a_hat0)])
+    g = math.prod(w) ** 0.25
+    a_bar = np.array([g / (g + 1), 1 / (g + 1)])
+    m = 0.5 * (a_hat + a_bar)
+    d_js = 0.5 * sum(a_hat * np.log(a_hat / m)) + 0.5 * sum(a_bar * np.log(a_bar / m))
+    np.testing.assert_allclose(a_hat, fx["a_hat"], rtol=1e-15)
+    np.testing.assert_allclose(a_bar, fx["a_bar"], rtol=1e-15)
+    assert abs(d_js - fx["d_js"]) < 1e-15
+    for case in fx["route_cases"]:
+        res = O.jsd_route(q, k, B, b, case["tau"])
+        np.testing.assert_allclose(res["a_hat"], a_hat, rtol=1e-13)
+        np.testing.assert_allclose(res["a_bar"], a_bar, rtol=1e-13)
+        assert abs(res["d_js"] - d_js) < 1e-14
+        assert res["route_vs"] == case["route_vs"]
