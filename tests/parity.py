@@ -19,6 +19,17 @@ TOL_REL = 1e-3
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
 REL_RMS = 1e-2
+# Bounds on what the exemption may cover (observed maxima so far: p error 3.4e-6 and 8
+# exempt PE pairs in a whole 512k layer, no exempt VS block or route):
+MAX_P_REL = 1e-4           # |p_gpu - p| / (p + 1e-6) of every VS head's pooled scores
+MAX_EXEMPT_PE_FRAC = 1e-4  # exempt pairs of one PE head / its N_b (N_b + 1) / 2 pairs
+MIN_EXEMPT_PE = 4          # ... but always allow this many
+MAX_EXEMPT_VS_FRAC = 1e-2  # exempt blocks of one VS head and direction / N_b
+MIN_EXEMPT_VS = 2          # ... but always allow this many
+MAX_EXEMPT_ROUTE_FRAC = 0.1  # exempt route mismatches / heads (and at least one allowed)
+
+# (workload, report) of every compare in this session, printed at the end of the run
+REPORTS = []
 
 
 def to_device(u16):
@@ -85,32 +96,58 @@ def _kth_largest(p, k):
     return p[order[k - 1]] if k >= 1 else np.inf
 
 
-def compare_selection(w, sel, osel, heads=None):
-    """Returns a report; raises AssertionError on any non-exempt mismatch."""
+def _oracle_head_forced(w, g, h, force):
+    params = O.workload_params(w)
+    q = O.bf16_bits_to_f64(g["q"][h])
+    k = O.bf16_bits_to_f64(g["k"][h // w.group])
+    r = O.crisp_select_head(q, k, force=force, **params)
+    r.pop("a_bar", None)
+    return r
+
+
+def compare_selection(w, sel, osel, heads=None, g=None):
+    """Returns a report; raises AssertionError on any non-exempt mismatch.
+
+    Every head's GPU CSR rows are checked: a VS head's rows must be exactly the union rule
+    (S_v u S_s u {0, I}, "Figures and tables", Algorithm 3) applied to the GPU's own block
+    sets, which in turn may differ from the oracle's only at exempt blocks; a PE head's
+    pairs may differ only where v lies within TOL_REL of the oracle's cut value.  The
+    counts of exempt items are bounded (MAX_EXEMPT_*), and so is the error of the pooled
+    scores p_v, p_s (MAX_P_REL).  A head whose route differs (C_struct within TOL_REL of
+    tau) is compared with the oracle forced to the GPU's route when the inputs g are given.
+    """
     nb = w.n_blocks
     heads = list(osel.keys()) if heads is None else heads
     gm = gpu_masks(sel, w.hq, nb)
     rep = dict(route_mismatch_exempt=0, vs_block_exempt=0, pe_pair_exempt=0, heads=len(heads),
-               vs_heads=0, pe_heads=0, max_cstruct_err=0.0, max_p_err=0.0, rows_checked=0)
+               vs_heads=0, pe_heads=0, max_cstruct_err=0.0, max_p_err=0.0, rows_checked=0,
+               max_vs_exempt_head=0, max_pe_exempt_head=0, mask_differs=[])
+    vs_cap = max(MIN_EXEMPT_VS, int(MAX_EXEMPT_VS_FRAC * nb))
+    pe_cap = max(MIN_EXEMPT_PE, int(MAX_EXEMPT_PE_FRAC * nb * (nb + 1) // 2))
     for h in heads:
         o = osel[h]
         gvs = bool(sel["route_vs"][h])
-        rep["max_cstruct_err"] = max(rep["max_cstruct_err"], abs(sel["c_struct"][h] - o["c_struct"]))
-        assert abs(sel["c_struct"][h] - o["c_struct"]) <= 1e-4 + 1e-4 * o["c_struct"], \
+        cerr = float(abs(sel["c_struct"][h] - o["c_struct"]))
+        rep["max_cstruct_err"] = max(rep["max_cstruct_err"], cerr)
+        assert cerr <= 1e-4 + 1e-4 * o["c_struct"], \
             f"head {h}: C_struct {sel['c_struct'][h]} vs oracle {o['c_struct']}"
         if gvs != o["route_vs"]:
             near = abs(o["c_struct"] - w.tau_proxy) <= TOL_REL * w.tau_proxy
             assert near, f"head {h}: route differs (C_struct {o['c_struct']})"
             rep["route_mismatch_exempt"] += 1
-            continue
+            rep["mask_differs"].append(h)
+            if g is None:
+                continue
+            o = _oracle_head_forced(w, g, h, "vs" if gvs else "pe")
         if gvs:
             rep["vs_heads"] += 1
-            exact = True
             for d, key in (("v", "sel_v"), ("s", "sel_s")):
                 p = o["p_" + d]
                 gp = sel["p_" + d][h]
                 err = np.abs(gp - p) / (np.abs(p) + 1e-6)
                 rep["max_p_err"] = max(rep["max_p_err"], float(err.max()))
+                assert err.max() <= MAX_P_REL, \
+                    f"head {h} dir {d}: pooled score error {err.max():.3g} at block {int(err.argmax())}"
                 gamma_rule = getattr(w, "vs_rule", "floor") == "gamma"
                 thr = w.alpha * o["mu_" + d]
                 osel_set = np.zeros(nb, bool)
@@ -124,11 +161,17 @@ def compare_selection(w, sel, osel, heads=None):
                         near |= abs(p[J] - kth) <= TOL_REL * kth
                     assert near, (f"head {h} dir {d}: block {J} differs (p={p[J]:.6g}, "
                                   f"thr={thr:.6g})")
-                    rep["vs_block_exempt"] += 1
-                    exact = False
-            if exact:
+                assert diff.size <= vs_cap, f"head {h} dir {d}: {diff.size} exempt blocks"
+                rep["vs_block_exempt"] += int(diff.size)
+                rep["max_vs_exempt_head"] = max(rep["max_vs_exempt_head"], int(diff.size))
+                if diff.size and h not in rep["mask_differs"]:
+                    rep["mask_differs"].append(h)
+            # the CSR rows are the union rule applied to the GPU's own sets
+            want = O.vs_block_mask(np.nonzero(sel["sel_v"][h])[0], np.nonzero(sel["sel_s"][h])[0], nb)
+            assert np.array_equal(gm[h], want), f"head {h}: VS CSR rows differ from S_v u S_s u {{0, I}}"
+            if h not in rep["mask_differs"]:
                 assert np.array_equal(gm[h], o["mask"]), f"head {h}: VS CSR rows differ"
-                rep["rows_checked"] += nb
+            rep["rows_checked"] += nb
         else:
             rep["pe_heads"] += 1
             diff = np.argwhere(np.tril(gm[h]) != np.tril(o["mask"]))
@@ -137,8 +180,16 @@ def compare_selection(w, sel, osel, heads=None):
                 vv = o["v"][I, K]
                 assert abs(vv - vstar) <= TOL_REL * vstar, \
                     f"head {h}: PE pair ({I},{K}) differs (v={vv:.6g}, v*={vstar:.6g})"
-                rep["pe_pair_exempt"] += 1
+            assert len(diff) <= pe_cap, f"head {h}: {len(diff)} exempt PE pairs (cap {pe_cap})"
+            rep["pe_pair_exempt"] += len(diff)
+            rep["max_pe_exempt_head"] = max(rep["max_pe_exempt_head"], len(diff))
+            if len(diff) and h not in rep["mask_differs"]:
+                rep["mask_differs"].append(h)
+            # every row holds its diagonal pair (the rescue rule)
+            assert gm[h][np.arange(nb), np.arange(nb)].all(), f"head {h}: PE row without its diagonal"
             rep["rows_checked"] += nb
+    assert rep["route_mismatch_exempt"] <= max(1, int(MAX_EXEMPT_ROUTE_FRAC * len(heads))), \
+        f"{rep['route_mismatch_exempt']} exempt route mismatches"
     return rep
 
 

@@ -7,8 +7,8 @@ the oracle's own index set must be within max abs 2e-2 / mean abs 2e-3 (tests/pa
 import numpy as np
 import pytest
 
-from tests.parity import (compare_outputs, compare_selection, csr_from_masks, gpu_masks,
-                          oracle_outputs, oracle_select, to_device)
+from tests.parity import (REPORTS, compare_outputs, compare_selection, csr_from_masks,
+                          gpu_masks, oracle_outputs, oracle_select, to_device)
 from workloads import get
 from workloads.configs import Workload
 from workloads.planted import generate, random_qkv
@@ -61,7 +61,7 @@ def run_parity(dsp, w, g, sample=None, seed=0, flags=0, report=None):
     if flags & dsp.FLAG_FORCE_PE:
         force = "pe"
     osel = oracle_select(w, g) if force is None else _oracle_forced(w, g, force)
-    rep = compare_selection(w, sel, osel)
+    rep = compare_selection(w, sel, osel, g=g)
 
     if sample is None:
         blocks = {h: list(range(nb)) for h in range(w.hq)}
@@ -85,19 +85,22 @@ def run_parity(dsp, w, g, sample=None, seed=0, flags=0, report=None):
         worst = [max(a, b) for a, b in zip(worst, r)]
     rep["attend_max_abs"], rep["attend_mean_abs"], rep["attend_rel_rms"] = worst
 
-    # (2) crisp_prefill's own output, for heads whose selection matched exactly
+    # (2) crisp_prefill's own output for every sampled head: against the rows above where
+    # the GPU selection equals the oracle's, else against the oracle's attention on the
+    # GPU's own selection (which compare_selection has validated item by item)
     got_p = o.float().cpu().numpy()
-    exact = 0
+    gmask = gpu_masks(sel, w.hq, nb)
+    differ = {h: bl for h, bl in blocks.items() if h in rep["mask_differs"]}
+    ref_g = oracle_outputs(w, g, {h: {"mask": gmask[h]} for h in differ}, differ) if differ else {}
     for h, bl in blocks.items():
-        gm = np.zeros((nb, nb), bool)
-        rpg, cg = sel["row_ptr"], sel["col"]
-        for I in range(nb):
-            gm[I, cg[rpg[h * nb + I]:rpg[h * nb + I + 1]]] = True
-        if np.array_equal(gm, np.tril(osel[h]["mask"])):
-            compare_outputs(got_p[h][_rows(bl)], ref[h], f"prefill, head {h}")
-            exact += 1
-    rep["prefill_heads_compared"] = exact
+        if h not in differ:
+            assert np.array_equal(gmask[h], np.tril(osel[h]["mask"])), h
+        compare_outputs(got_p[h][_rows(bl)], ref_g[h] if h in differ else ref[h],
+                        f"prefill, head {h}")
+    rep["prefill_heads_compared"] = len(blocks)
+    rep["prefill_heads_on_gpu_selection"] = len(differ)
     ctx.close()
+    REPORTS.append((f"{w.name} n={w.n} hq={w.hq} alpha={w.alpha} flags={flags:#x}", dict(rep)))
     if report is not None:
         report.update(rep)
     return rep, sel, osel
