@@ -32,6 +32,10 @@ bool dims_valid(const crisp_dims* d) {
          d->hq % d->hkv == 0;
 }
 
+}  // namespace
+
+namespace crisp {
+
 crisp_status check_dims(const crisp_dims* d) {
   if (!dims_valid(d)) return CRISP_ERR_INVALID_ARG;
   if (d->d != kD) return CRISP_ERR_UNSUPPORTED;
@@ -54,6 +58,10 @@ crisp_status check_cfg(const crisp_cfg* c) {
     return CRISP_ERR_INVALID_ARG;
   return CRISP_OK;
 }
+
+}  // namespace crisp
+
+namespace {
 
 bool fits(const crisp_ctx ctx, const crisp_dims* d) {
   const int64_t H = static_cast<int64_t>(d->batch) * d->hq;

@@ -125,6 +125,10 @@ struct crisp_ctx_s {
 namespace crisp {
 
 Shape make_shape(const crisp_dims& d);
+// The shape and parameter rules of include/crisp.h (CRISP_OK, CRISP_ERR_INVALID_ARG or
+// CRISP_ERR_UNSUPPORTED); host only.
+crisp_status check_dims(const crisp_dims* d);
+crisp_status check_cfg(const crisp_cfg* c);
 
 // Each launcher only enqueues work on `st` and returns the launch status.
 cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,

@@ -784,38 +784,44 @@ StaticSetup g_static_setup[kMaxDevices];
 std::mutex g_static_mu;
 
 // Once per device, with that device current: resolve the scratch address and the other
-// per-device state.  Allocates nothing.
+// per-device state.  Allocates nothing.  Only a completed setup is kept (and the permanent
+// answer for a device of another architecture); a failure of any step leaves the device
+// unset, so the next call tries again.
 crisp_status static_setup(int dev, StaticSetup** out) {
   if (dev < 0 || dev >= kMaxDevices) return CRISP_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_static_mu);
   StaticSetup& s = g_static_setup[dev];
-  if (!s.done) {
-    s.done = true;
-    int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (major != 10 || minor != 3) {
-      s.status = CRISP_ERR_UNSUPPORTED;
-    } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.scratch), g_route_scratch) !=
-                   cudaSuccess ||
-               !s.scratch) {
-      s.status = CRISP_ERR_CUDA;
-    } else if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                cudaEnableDefault, &q) != cudaSuccess ||
-               q != cudaDriverEntryPointSuccess || !fn) {
-      s.status = CRISP_ERR_CUDA;
-    } else if (init_patsearch_attributes() != cudaSuccess) {
-      s.status = CRISP_ERR_CUDA;
-    } else {
-      s.encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
-    if (s.status != CRISP_OK) cudaGetLastError();
-  }
   *out = &s;
-  return s.status;
+  if (s.done) return s.status;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return CRISP_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) {  // the kernels are built for sm_103a only
+    s.status = CRISP_ERR_UNSUPPORTED;
+    s.done = true;
+    return s.status;
+  }
+  unsigned char* scratch = nullptr;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&scratch), g_route_scratch) != cudaSuccess ||
+      !scratch ||
+      cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn || init_patsearch_attributes() != cudaSuccess) {
+    cudaGetLastError();
+    return CRISP_ERR_CUDA;
+  }
+  s.scratch = scratch;
+  s.encode = reinterpret_cast<EncodeTiledFn>(fn);
+  s.num_sms = sms;
+  s.status = CRISP_OK;
+  s.done = true;
+  return CRISP_OK;
 }
 
 bool static_map(EncodeTiledFn encode, CUtensorMap* map, const void* base, int64_t rows) {
@@ -838,15 +844,10 @@ extern "C" crisp_status crisp_route_static(const crisp_dims* dims, const void* Q
   using namespace crisp;
   if (!dims || !cfg || !Q || !K || !route_vs || !c_struct || !status)
     return CRISP_ERR_INVALID_ARG;
-  if (dims->batch < 1 || dims->n < 1 || dims->hq < 1 || dims->hkv < 1 || dims->hq % dims->hkv)
-    return CRISP_ERR_INVALID_ARG;
-  if (dims->d != kD || dims->n % kBlk != 0) return CRISP_ERR_UNSUPPORTED;
-  if (cfg->B != kBlk || cfg->b != kBlk || cfg->w_sink < 1 || cfg->w_sink > kBlk ||
-      cfg->w_local < 1 || cfg->w_local > kBlk)
-    return CRISP_ERR_UNSUPPORTED;
-  if (!(cfg->alpha >= 0.f) || cfg->k_min_tokens < 0 || !(cfg->tau_proxy == cfg->tau_proxy) ||
-      ((cfg->flags & CRISP_FLAG_FORCE_VS) && (cfg->flags & CRISP_FLAG_FORCE_PE)))
-    return CRISP_ERR_INVALID_ARG;
+  // The shape and parameter rules of crisp_select, then the scratch limits.
+  crisp_status chk = check_dims(dims);
+  if (chk == CRISP_OK) chk = check_cfg(cfg);
+  if (chk != CRISP_OK) return chk;
   if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K)) & 15u)
     return CRISP_ERR_INVALID_ARG;
   const Shape s = make_shape(*dims);

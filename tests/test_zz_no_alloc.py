@@ -86,3 +86,13 @@ def test_route_static_rejects_sizes_beyond_its_scratch(dsp):
                                           ctypes.c_void_p(cs.data_ptr()),
                                           ctypes.c_void_p(status.data_ptr()), None)
         assert st == 2  # CRISP_ERR_UNSUPPORTED, before any work is queued
+    # parameters crisp_select refuses are refused here too (CRISP_ERR_INVALID_ARG)
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    for bad in (dsp.default_cfg(gamma=0.0), dsp.default_cfg(gamma=1.5),
+                dsp.default_cfg(flags=dsp.FLAG_MEDIAN_FLOOR | dsp.FLAG_VS_GAMMA_CUMSUM)):
+        st = dsp.lib().crisp_route_static(ctypes.byref(dims), ctypes.c_void_p(q.data_ptr()),
+                                          ctypes.c_void_p(k.data_ptr()), ctypes.byref(bad),
+                                          ctypes.c_void_p(out.data_ptr()),
+                                          ctypes.c_void_p(cs.data_ptr()),
+                                          ctypes.c_void_p(status.data_ptr()), None)
+        assert st == 1
