@@ -46,39 +46,6 @@ def algorithmic_flops(nnz: int, rows: int) -> float:
     return 4.0 * B * B * D * (nnz - rows) + 2.0 * D * B * (B + 1) * rows
 
 
-def kernel_code_hash(path: str) -> str:
-    """sha256 of a CUDA source with // comments and blank lines removed: the counters of a
-    capture stay valid while only the comments change."""
-    import hashlib
-    import re
-    lines = []
-    for line in open(path).read().splitlines():
-        line = re.sub(r"//.*$", "", line).rstrip()
-        if line.strip():
-            lines.append(line)
-    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
-
-
-def recorded_traffic(workload: str):
-    """DRAM bytes of one crisp_attend (summed over its attention-kernel launches) from the
-    committed ncu summary, if it was taken on this workload with the current kernel code;
-    else None."""
-    import re
-    prof = os.path.join(ROOT, "profiles", f"attention_kernel_{workload}_traffic.md")
-    src = os.path.join(ROOT, "dynamic_sparse_prefill_gb300", "csrc", "attention.cu")
-    if not os.path.exists(prof):
-        return None
-    text = open(prof).read()
-    m = re.search(r"code_sha256: ([0-9a-f]{64})", text)
-    rd = re.search(r"dram_bytes_read: (\d+)", text)
-    wr = re.search(r"dram_bytes_write: (\d+)", text)
-    if not (m and rd and wr):
-        return None
-    if kernel_code_hash(src) != m.group(1):
-        return None
-    return int(rd.group(1)) + int(wr.group(1))
-
-
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -146,8 +113,10 @@ def make_inputs(w):
 
 def cpu_oracle_sample(w, g, stats, budget_s=20.0):
     """Times the fp64 CPU oracle on a bounded sample of the workload and extrapolates to
-    one layer: full selection of one VS-planted and one PE-planted head, and the exact
-    attention of a few query blocks (per selected block pair)."""
+    one layer: the full selection of one VS-planted and one PE-planted head, and the exact
+    attention of sampled query blocks of both heads, timed per selected block pair
+    separately for VS rows (a few tens of scattered blocks) and PE rows (long runs), then
+    weighted by the layer's VS and PE pair counts (stats: n_vs, n_pe, nnz_vs, nnz_pe)."""
     from oracle import crisp_oracle as O
     params = O.workload_params(w)
     pe_set = set(w.pe_heads)
@@ -161,36 +130,42 @@ def cpu_oracle_sample(w, g, stats, budget_s=20.0):
         t0 = time.perf_counter()
         sels[h] = O.crisp_select_head(q, k, **params)
         t_sel[h] = time.perf_counter() - t0
-    # attention: sampled query blocks of the PE head (long rows) until ~budget/2 seconds
-    h = pe_h if pe_h is not None else vs_h
-    q = O.bf16_bits_to_f64(g["q"][h])
-    k = O.bf16_bits_to_f64(g["k"][h // w.group])
-    v = O.bf16_bits_to_f64(g["v"][h // w.group])
-    mask = sels[h]["mask"]
     rng = np.random.default_rng(5)
     nb = w.n_blocks
-    pairs, t_att, blocks = 0, 0.0, 0
-    t_start = time.perf_counter()
-    while time.perf_counter() - t_start < budget_s / 2 and blocks < nb:
-        I = int(rng.integers(nb // 2, nb))
-        t0 = time.perf_counter()
-        O.block_sparse_attention(q, k, v, mask, w.B, [I])
-        t_att += time.perf_counter() - t0
-        pairs += int(mask[I, : I + 1].sum())
-        blocks += 1
-    per_pair = t_att / max(pairs, 1)
-    n_pe = stats["n_pe"]
-    n_vs = stats["n_vs"]
+    per_pair, desc, t_att_total = {}, [], 0.0
+    heads = [("vs", vs_h)] + ([("pe", pe_h)] if pe_h is not None else [])
+    for kind, h in heads:
+        q = O.bf16_bits_to_f64(g["q"][h])
+        k = O.bf16_bits_to_f64(g["k"][h // w.group])
+        v = O.bf16_bits_to_f64(g["v"][h // w.group])
+        mask = sels[h]["mask"]
+        pairs, t_att, blocks = 0, 0.0, 0
+        t_start = time.perf_counter()
+        while time.perf_counter() - t_start < budget_s / (2 * len(heads)) and blocks < nb:
+            I = int(rng.integers(nb // 2, nb))
+            t0 = time.perf_counter()
+            O.block_sparse_attention(q, k, v, mask, w.B, [I])
+            t_att += time.perf_counter() - t0
+            pairs += int(mask[I, : I + 1].sum())
+            blocks += 1
+        per_pair[kind] = t_att / max(pairs, 1)
+        t_att_total += t_att
+        desc.append(f"exact attention of {blocks} query blocks of head {h} ({kind.upper()}, "
+                    f"{pairs} block pairs, {t_att:.2f} s)")
+    n_pe, n_vs = stats["n_pe"], stats["n_vs"]
+    nnz_vs = stats.get("nnz_vs", stats["nnz"] if pe_h is None else 0)
+    nnz_pe = stats.get("nnz_pe", stats["nnz"] - nnz_vs)
     sel_s = t_sel[vs_h] * n_vs + (t_sel[pe_h] if pe_h is not None else t_sel[vs_h]) * n_pe
-    total_s = sel_s + per_pair * stats["nnz"]
+    att_s = per_pair["vs"] * nnz_vs + per_pair.get("pe", per_pair["vs"]) * nnz_pe
+    total_s = sel_s + att_s
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"oracle selection of head {vs_h} (VS) and head {pe_h} (PE) in full "
-              f"({t_sel[vs_h]:.2f} s, {t_sel.get(pe_h, 0):.2f} s); exact attention of "
-              f"{blocks} query blocks ({pairs} block pairs, {t_att:.2f} s); extrapolated "
-              f"to {n_vs} VS + {n_pe} PE heads and {stats['nnz']} block pairs")
+              f"({t_sel[vs_h]:.2f} s, {t_sel.get(pe_h, 0):.2f} s); " + "; ".join(desc) +
+              f"; extrapolated per block pair to {n_vs} VS + {n_pe} PE heads with "
+              f"{nnz_vs} VS and {nnz_pe} PE block pairs")
     return {"value": total_s * 1e3, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": sample, "extrapolated": True,
-            "measured_s": sum(t_sel.values()) + t_att}
+            "measured_s": sum(t_sel.values()) + t_att_total}
 
 
 def run_reference(args, w, rank, world):
@@ -209,13 +184,14 @@ def run_reference(args, w, rank, world):
         # the layer's pair count is estimated from those two heads' masks.
         vs_h = next(h for h in range(w.hq) if h not in pe_set)
         pe_h = next((h for h in range(w.hq) if h in pe_set), vs_h)
-        nnz = 0
-        for h, mult in ((vs_h, w.hq - n_pe), (pe_h, n_pe)):
+        nnz = {}
+        for kind, h, mult in (("vs", vs_h, w.hq - n_pe), ("pe", pe_h, n_pe)):
             q = O.bf16_bits_to_f64(g["q"][h])
             k = O.bf16_bits_to_f64(g["k"][h // w.group])
             r = O.crisp_select_head(q, k, **params)
-            nnz += int(np.tril(r["mask"]).sum()) * mult
-        stats = {"n_vs": w.hq - n_pe, "n_pe": n_pe, "nnz": nnz}
+            nnz[kind] = int(np.tril(r["mask"]).sum()) * mult
+        stats = {"n_vs": w.hq - n_pe, "n_pe": n_pe, "nnz": nnz["vs"] + nnz["pe"],
+                 "nnz_vs": nnz["vs"], "nnz_pe": nnz["pe"]}
         cb = cpu_oracle_sample(w, g, stats, budget_s=args.ref_budget)
         if step >= args.warmup:
             vals.append(cb["value"])
@@ -225,7 +201,7 @@ def run_reference(args, w, rank, world):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": value, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (planted, seeded)",
-            "config": workload_config(w), "cpu_baseline": cb,
+            "config": dict(workload_config(w), vs_variant=args.vs_variant), "cpu_baseline": cb,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -265,6 +241,127 @@ def replica_value(ms_per_step: float, world: int) -> float:
     return ms_per_step / world
 
 
+def route_pair_counts(ctx, dims, nb):
+    """Selected block pairs of the context's selection on VS-routed and PE-routed heads."""
+    sel = ctx.selection_get(dims, with_csr=False)
+    rp = sel["row_ptr"]
+    per_head = rp[nb::nb] - rp[:-1:nb]
+    vs = sel["route_vs"].astype(bool)
+    return int(per_head[vs].sum()), int(per_head[~vs].sum())
+
+
+def timed_steps(ctx, dims, q, k, v, o, cfg, steps, stream):
+    """`steps` back-to-back crisp_select + crisp_attend on `stream` (CUDA events):
+    (total ms, mean select ms, mean attend ms)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        ctx.select(dims, q, k, cfg)
+        ev[i][1].record(stream)
+        ctx.attend(dims, q, k, v, o)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return (t0.elapsed_time(t1), statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
+            statistics.mean(e[1].elapsed_time(e[2]) for e in ev))
+
+
+def timed_dense(ctx, dims, q, k, v, o, steps, stream):
+    import torch
+    ctx.dense(dims, q, k, v, o)
+    torch.cuda.synchronize()
+    de = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    de[0].record(stream)
+    for _ in range(steps):
+        ctx.dense(dims, q, k, v, o)
+    de[1].record(stream)
+    torch.cuda.synchronize()
+    if ctx.sync_status() != 0:
+        raise RuntimeError("device error in dense attention")
+    return de[0].elapsed_time(de[1]) / steps
+
+
+def e2e_host(ctx, dims, cfg, g, q, k, v, o, calls, stream):
+    """The same layer through crisp_prefill_host from pinned host buffers (uploads of Q, K,
+    V and the download of O inside the timed region, overlapped chunk by chunk), `calls`
+    calls after one untimed call; plus the copies alone (one H2D of Q, K, V and one D2H of
+    O, back to back on the stream) for the achieved copy bandwidth."""
+    import torch
+    qh = torch.from_numpy(g["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    kh = torch.from_numpy(g["k"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    vh = torch.from_numpy(g["v"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = int(qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = int(oh.numel()) * 2
+    ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q, k, v, o)
+    torch.cuda.synchronize()
+    per_call = []
+    for _ in range(calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q, k, v, o)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per_call.append(e0.elapsed_time(e1))
+    if ctx.sync_status() != 0:
+        raise RuntimeError("device error in the end-to-end run")
+    c = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    c[0].record(stream)
+    q.copy_(qh, non_blocking=True)
+    k.copy_(kh, non_blocking=True)
+    v.copy_(vh, non_blocking=True)
+    c[1].record(stream)
+    oh.copy_(o, non_blocking=True)
+    c[2].record(stream)
+    torch.cuda.synchronize()
+    h2d_ms, d2h_ms = c[0].elapsed_time(c[1]), c[1].elapsed_time(c[2])
+    del qh, kh, vh, oh
+    return {"per_call_ms": per_call, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+            "copies_alone_ms": h2d_ms + d2h_ms}
+
+
+def point_128k(dsp, w, g, steps, warmup, dense_steps, dev, stream):
+    """select, attend and layer ms, effective TFLOP/s and the dense speedup of one 128k
+    workload (device-resident inputs, same timing as the headline)."""
+    import torch
+
+    def dev_tensor(u16):
+        return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = dev_tensor(g["q"]), dev_tensor(g["k"]), dev_tensor(g["v"])
+    o = torch.empty_like(q)
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    ctx = dsp.Context(dims)
+    cfg = dsp.default_cfg(alpha=w.alpha, gamma=w.gamma, tau_proxy=w.tau_proxy,
+                          k_min_tokens=w.k_min_tokens)
+    for _ in range(warmup):
+        ctx.prefill(dims, q, k, v, cfg, o)
+    if ctx.sync_status() != 0:
+        raise RuntimeError(f"device error during warm-up of {w.name}")
+    st = ctx.stats(dims)
+    total, sel_ms, att_ms = timed_steps(ctx, dims, q, k, v, o, cfg, steps, stream)
+    if ctx.sync_status() != 0:
+        raise RuntimeError(f"device error in {w.name}")
+    dense_ms = timed_dense(ctx, dims, q, k, v, o, dense_steps, stream)
+    ctx.close()
+    nbk = w.n // B
+    flops = algorithmic_flops(st["nnz"], st["rows"])
+    ms = total / steps
+    return {"n": w.n, "hq": w.hq, "hkv": w.hkv, "alpha": w.alpha, "ms_per_layer": ms,
+            "select_ms": sel_ms, "attend_ms": att_ms,
+            "tflops_effective": flops / (ms * 1e-3) / 1e12,
+            "attend_tflops": flops / (att_ms * 1e-3) / 1e12, "dense_ms": dense_ms,
+            "dense_tflops": algorithmic_flops(w.hq * nbk * (nbk + 1) // 2, w.hq * nbk)
+            / (dense_ms * 1e-3) / 1e12,
+            "speedup_vs_dense": dense_ms / ms,
+            "density": st["nnz"] / (w.hq * nbk * (nbk + 1) / 2),
+            "n_vs": st["n_vs"], "n_pe": st["n_pe"], "steps": steps, "warmup": warmup}
+
+
 def run_gpu(args, w, rank, world):
     import torch
     import torch.distributed as dist
@@ -292,68 +389,46 @@ def run_gpu(args, w, rank, world):
     if ctx.sync_status() != 0:
         raise RuntimeError("device error during warm-up")
     stats = ctx.stats(dims)
+    stats["nnz_vs"], stats["nnz_pe"] = route_pair_counts(ctx, dims, w.n // B)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            ctx.select(dims, q, k, cfg)
-            ev[i][1].record(stream)
-            ctx.attend(dims, q, k, v, o)
-            ev[i][2].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        total_ms, sel_ms, att_ms = timed_steps(ctx, dims, q, k, v, o, cfg, args.steps, stream)
     if world > 1:
         dist.barrier()
     if ctx.sync_status() != 0:
         raise RuntimeError("device error during the timed region")
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
-    sel_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
     value = replica_value(ms_per_step, world)
 
-    # end to end through the public API with host buffers (pinned), copies included:
-    # crisp_prefill_host uploads, computes and downloads chunk by chunk, overlapped
-    qh = torch.from_numpy(g["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    kh = torch.from_numpy(g["k"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    vh = torch.from_numpy(g["v"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    oh = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(1, min(args.steps, 3))
-    ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q, k, v, o)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        ctx.prefill_host(dims, qh, kh, vh, cfg, oh, q, k, v, o)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if ctx.sync_status() != 0:
-        raise RuntimeError("device error in the end-to-end run")
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = int(qh.numel() + kh.numel() + vh.numel()) * 2
-    d2h = int(oh.numel()) * 2
+    # end to end through the public API with host buffers (pinned), copies included
+    e2e = e2e_host(ctx, dims, cfg, g, q, k, v, o, max(5, min(args.steps, 8)), stream)
+    e2e_ms = statistics.mean(e2e["per_call_ms"])
 
     # dense causal attention on the same inputs (the speedup denominator)
-    dense_ms = None
-    if not args.no_dense:
-        ctx.dense(dims, q, k, v, o)
-        torch.cuda.synchronize()
-        de = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        de[0].record(stream)
-        for _ in range(args.dense_steps):
-            ctx.dense(dims, q, k, v, o)
-        de[1].record(stream)
-        torch.cuda.synchronize()
-        dense_ms = de[0].elapsed_time(de[1]) / args.dense_steps
-        if ctx.sync_status() != 0:
-            raise RuntimeError("device error in dense attention")
+    dense_ms = None if args.no_dense else timed_dense(ctx, dims, q, k, v, o, args.dense_steps,
+                                                      stream)
+    ctx.close()
+    del q, k, v, o
+
+    # the metric's 128k point: the Llama-3-8B layer at alpha = 1.0 and 1.25, and the
+    # Qwen2-7B layer, each after the headline's timed region
+    at_128k = None
+    if not args.no_128k:
+        from workloads import get
+        at_128k = {}
+        g128 = None
+        for name in ("llama8b_n128k_a1", "llama8b_n128k_a125", "qwen7b_n128k"):
+            w1 = get(name)
+            if g128 is None or g128[0] != (w1.seed, w1.hq, w1.hkv, w1.n):
+                g128 = ((w1.seed, w1.hq, w1.hkv, w1.n), make_inputs(w1))
+            at_128k[name] = point_128k(dsp, w1, g128[1], args.steps_128k, 2,
+                                       args.dense_steps, dev, stream)
+        del g128
+        torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -361,8 +436,31 @@ def run_gpu(args, w, rank, world):
     flops = algorithmic_flops(stats["nnz"], stats["rows"])
     att_tflops = flops / (att_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    clocks = clk.summary()
+    peak_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    run_mhz = clocks.get("sm_mhz")
     nbk = w.n // B
     dense_flops = algorithmic_flops(w.hq * nbk * (nbk + 1) // 2, w.hq * nbk)
+    roofline = {
+        "kernel": "attention_kernel", "bound": "tensor", "achieved": att_tflops,
+        "peak": peak, "unit": "TFLOP/s", "frac": att_tflops / peak,
+        "peak_kind": f"bf16 sustained (cuBLAS, seconds-long loop), {peak_kind}",
+        "unit_of_work": "one crisp_attend call (all launches of the attention kernels for "
+                        "the layer)",
+        "algorithmic_flops_per_attend": flops,
+        "traffic": None,
+        "traffic_note": "DRAM bytes are not counted in this run; they come from ncu "
+                        "captures of one attention launch at 32k tokens, scaled by units",
+    }
+    if peak_mhz and run_mhz:
+        # the measured peak was taken at its own median SM clock; scaled to this run's
+        roofline["peak_sm_mhz"] = peak_mhz
+        roofline["run_sm_mhz"] = run_mhz
+        roofline["peak_at_run_clock"] = peak * run_mhz / peak_mhz
+        roofline["frac_at_run_clock"] = att_tflops / roofline["peak_at_run_clock"]
+        roofline["frac_basis"] = ("frac: against the measured sustained peak as recorded; "
+                                  "frac_at_run_clock: that peak scaled by this run's median "
+                                  "SM clock over the peak's")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False,
@@ -377,24 +475,25 @@ def run_gpu(args, w, rank, world):
         "selection": {"nnz_block_pairs": stats["nnz"], "rows": stats["rows"],
                       "density": stats["nnz"] / (w.hq * nbk * (nbk + 1) / 2),
                       "n_vs": stats["n_vs"], "n_pe": stats["n_pe"],
+                      "nnz_vs": stats["nnz_vs"], "nnz_pe": stats["nnz_pe"],
                       "pe_rescued_rows": stats["pe_rescued"], "max_row": stats["max_row"]},
-        "roofline": {"kernel": "attention_kernel", "bound": "tensor", "achieved": att_tflops,
-                     "peak": peak, "unit": "TFLOP/s", "frac": att_tflops / peak,
-                     "peak_kind": f"bf16 sustained, {peak_kind}",
-                     "traffic": recorded_traffic(w.name),
-                     "unit_of_work": "one crisp_attend call (all launches of the attention "
-                                     "kernels for the layer)",
-                     "algorithmic_flops_per_attend": flops},
+        "roofline": roofline,
         "gpu_launches": launches_per_prefill(w, torch.cuda.get_device_properties(0).multi_processor_count) * args.steps,
-        "e2e": {"value": e2e_ms / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "clocks": clk.summary(),
+        "e2e": {"value": e2e_ms / world, "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "calls": len(e2e["per_call_ms"]),
+                "per_call_ms": [round(x, 2) for x in e2e["per_call_ms"]],
+                "h2d_gbs": e2e["h2d_gbs"], "d2h_gbs": e2e["d2h_gbs"],
+                "copies_alone_ms": e2e["copies_alone_ms"],
+                "exposed_over_device_ms": e2e_ms - ms_per_step},
+        "clocks": clocks,
+        "at_128k": at_128k,
         "pages_context": {"crisp_speedup_vs_flashattention_512k_h100": 5.30},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(w, g, stats, budget_s=args.ref_budget)
     print(json.dumps(line), flush=True)
-    ctx.close()
 
 
 def run_sweep(args):
@@ -532,6 +631,9 @@ def main():
     ap.add_argument("--dense-steps", type=int, default=2)
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-128k", action="store_true",
+                    help="skip the 128k points (Llama alpha 1.0 / 1.25, Qwen) after the headline")
+    ap.add_argument("--steps-128k", type=int, default=5)
     ap.add_argument("--ref-budget", type=float, default=12.0)
     ap.add_argument("--vs-variant", default="none", choices=["none", "median", "gamma"],
                     help="VS selection variant: median noise floor, or FlexPrefill's "

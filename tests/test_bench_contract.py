@@ -23,9 +23,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["higher_is_better"] is False and d["unit"] == "ms/layer"
     assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["config"]["workload"] == "tiny_n4k"
+    assert d["config"]["vs_variant"] == "none"   # the GPU arm's config carries the same keys
     assert d["value"] > 0 and d["ms_per_step"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
-    assert cb["sample"]
+    assert cb["sample"] and "VS" in cb["sample"] and "PE" in cb["sample"]
