@@ -54,7 +54,8 @@ class SelectionHost(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [("nnz", ctypes.c_int64), ("rows", ctypes.c_int64), ("max_row", ctypes.c_int64),
                 ("pe_rescued", ctypes.c_int64), ("n_vs", ctypes.c_int32),
-                ("n_pe", ctypes.c_int32)]
+                ("n_pe", ctypes.c_int32), ("near_routes", ctypes.c_int32),
+                ("near_vs_blocks", ctypes.c_int64), ("near_pe_pairs", ctypes.c_int64)]
 
 
 class CrispError(RuntimeError):

@@ -290,6 +290,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.route), static_cast<size_t>(H)},
       {reinterpret_cast<void**>(&w.mu), sizeof(float) * H * 2},
       {reinterpret_cast<void**>(&w.counts), sizeof(int32_t) * H * 4},
+      {reinterpret_cast<void**>(&w.near), sizeof(int32_t) * H * 3},
       {reinterpret_cast<void**>(&w.selv), static_cast<size_t>(H * nb)},
       {reinterpret_cast<void**>(&w.sels), static_cast<size_t>(H * nb)},
       {reinterpret_cast<void**>(&w.qs), sizeof(uint16_t) * 2 * H * nb * kD},
@@ -367,10 +368,16 @@ crisp_status crisp_select(crisp_ctx ctx, const crisp_dims* dims, const void* Q, 
   memset(&tmO, 0, sizeof(tmO));
   const bool tma_out = (s.nb % 4) == 0;
   if (tma_out && (st = make_prob_map(ctx, &tmO, ctx->ws.pev, s.nb, s.H)) != CRISP_OK) return st;
-  if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, tmQs, tmKs, tmO, tma_out, cs),
-                     "pe_index")) != CRISP_OK)
-    return st;
-  if ((st = launched(ctx, launch_build_csr(ctx, s, cs), "build_csr")) != CRISP_OK) return st;
+  {
+    PhaseRange r("PE");
+    if ((st = launched(ctx, launch_pe_index(ctx, s, *cfg, Q, K, tmQs, tmKs, tmO, tma_out, cs),
+                       "pe_index")) != CRISP_OK)
+      return st;
+  }
+  {
+    PhaseRange r("CSR");
+    if ((st = launched(ctx, launch_build_csr(ctx, s, cs), "build_csr")) != CRISP_OK) return st;
+  }
   ctx->has_sel = true;
   ctx->has_patsearch = true;
   ctx->sel_dims = *dims;
@@ -672,10 +679,11 @@ crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* 
   const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
   std::vector<int64_t> rp(rows + 1);
   std::vector<uint8_t> route(s.H);
-  std::vector<int32_t> counts(4 * s.H);
+  std::vector<int32_t> counts(4 * s.H), near(3 * s.H);
   if ((st = copy_out(ctx, rp.data(), ctx->ws.row_ptr, (rows + 1) * 8)) != CRISP_OK) return st;
   if ((st = copy_out(ctx, route.data(), ctx->ws.route, s.H)) != CRISP_OK) return st;
   if ((st = copy_out(ctx, counts.data(), ctx->ws.counts, 16 * s.H)) != CRISP_OK) return st;
+  if ((st = copy_out(ctx, near.data(), ctx->ws.near, 12 * s.H)) != CRISP_OK) return st;
   out->nnz = rp[rows];
   out->rows = rows;
   out->max_row = 0;
@@ -684,7 +692,13 @@ crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* 
   out->n_vs = 0;
   out->n_pe = 0;
   out->pe_rescued = 0;
+  out->near_routes = 0;
+  out->near_vs_blocks = 0;
+  out->near_pe_pairs = 0;
   for (int h = 0; h < s.H; ++h) {
+    out->near_routes += near[3 * h];
+    out->near_vs_blocks += near[3 * h + 1];
+    out->near_pe_pairs += near[3 * h + 2];
     if (route[h]) {
       ++out->n_vs;
     } else {

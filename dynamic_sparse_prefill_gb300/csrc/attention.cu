@@ -1091,6 +1091,7 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   const int per = attention_kv_heads_per_launch(s, ctx->num_sms);
   const int nlaunch = (s.Hkv + per - 1) / per;
   if (!dense) {
+    PhaseRange range("work order");
     const int rows = s.H * s.nb;
     const int nbins = nlaunch * (s.nb + 1);
     cudaError_t e = cudaMemsetAsync(ctx->ws.len_hist, 0, sizeof(int) * nbins, st);
@@ -1110,6 +1111,7 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   a.list_count = nullptr;
   a.redo = ctx->ws.redo;
   a.redo_count = ctx->ws.redo_count;
+  PhaseRange range("attention");
   cudaError_t e = cudaMemsetAsync(ctx->ws.redo_count, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(ctx->ws.work_ctr, 0, sizeof(int) * nlaunch, st);

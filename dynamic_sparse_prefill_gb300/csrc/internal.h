@@ -8,6 +8,8 @@
 
 #include "crisp.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace crisp {
 
 constexpr int kD = 128;        // head dimension
@@ -46,6 +48,7 @@ struct Workspace {
   uint8_t* route = nullptr;  // [H] 1 = VS
   float* mu = nullptr;       // [H][2]
   int32_t* counts = nullptr; // [H][4]
+  int32_t* near = nullptr;   // [H][3] near-threshold route, VS blocks, PE pairs (crisp_stats)
   uint8_t* selv = nullptr;   // [H][nb]
   uint8_t* sels = nullptr;   // [H][nb]
   // PEIndex
@@ -125,6 +128,29 @@ struct crisp_ctx_s {
 namespace crisp {
 
 Shape make_shape(const crisp_dims& d);
+
+// An NVTX range in the library's "crisp" domain for the launches of one phase (PatSearch,
+// VS, PE, CSR, work order, attention); costs nothing unless a profiler is attached.
+class PhaseRange {
+ public:
+  explicit PhaseRange(const char* name) {
+    nvtxEventAttributes_t ev = {};
+    ev.version = NVTX_VERSION;
+    ev.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    ev.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    ev.message.ascii = name;
+    nvtxDomainRangePushEx(domain(), &ev);
+  }
+  ~PhaseRange() { nvtxDomainRangePop(domain()); }
+  PhaseRange(const PhaseRange&) = delete;
+  PhaseRange& operator=(const PhaseRange&) = delete;
+
+ private:
+  static nvtxDomainHandle_t domain() {
+    static nvtxDomainHandle_t d = nvtxDomainCreateA("crisp");
+    return d;
+  }
+};
 // The shape and parameter rules of include/crisp.h (CRISP_OK, CRISP_ERR_INVALID_ARG or
 // CRISP_ERR_UNSUPPORTED); host only.
 crisp_status check_dims(const crisp_dims* d);

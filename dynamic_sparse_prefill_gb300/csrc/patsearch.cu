@@ -384,6 +384,7 @@ struct RouteArgs {
   uint8_t* route;
   float* mu;
   int32_t* counts;
+  int32_t* near;  // [H][3]: near-threshold route, VS blocks, (PE pairs: pe_index.cu)
   uint8_t* selv;
   uint8_t* sels;
 };
@@ -398,6 +399,19 @@ __device__ float block_sum_1024(float x, float* red) {
   float t = lane < (blockDim.x >> 5) ? red[lane] : 0.f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+__device__ float block_min_1024(float x, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  __syncthreads();
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  float t = lane < (blockDim.x >> 5) ? red[lane] : FLT_MAX;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t = fminf(t, __shfl_xor_sync(0xffffffffu, t, o));
   return t;
 }
 
@@ -595,6 +609,11 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
     a.cstruct[h] = C;
     a.route[h] = vs ? 1 : 0;
     for (int i = 0; i < 4; ++i) a.counts[h * 4 + i] = 0;
+    // near-threshold counts: the route's here, the VS blocks' below, the PE pairs' in the
+    // PE mask kernel
+    a.near[h * 3 + 0] = fabsf(C - a.tau) <= 1e-3f * fabsf(a.tau) ? 1 : 0;
+    a.near[h * 3 + 1] = 0;
+    a.near[h * 3 + 2] = 0;
   }
   if (!vs) {
     for (int J = threadIdx.x; J < nb; J += blockDim.x) {
@@ -627,11 +646,33 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
     select_direction(sps, sss, nb, a.alpha * mu_s, a.kmin_blocks, red, redf, &cs, &ks);
   }
   __syncthreads();
+  // Near-threshold blocks: within 1e-3 of alpha * mu_d (floor rule), or of the smallest kept
+  // score where the k_min padding (or the gamma-cumsum rule) decided the set.
+  const bool gamma_rule = (a.flags & CRISP_FLAG_VS_GAMMA_CUMSUM) != 0;
+  const bool pad_v = gamma_rule || kv > cv, pad_s = gamma_rule || ks > cs;
+  float kth_v = FLT_MAX, kth_s = FLT_MAX;
+  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+    if (ssv[J]) kth_v = fminf(kth_v, spv[J]);
+    if (sss[J]) kth_s = fminf(kth_s, sps[J]);
+  }
+  kth_v = block_min_1024(kth_v, redf);
+  kth_s = block_min_1024(kth_s, redf);
+  const float thr_v = a.alpha * mu_v, thr_s = a.alpha * mu_s;
+  int near = 0;
+  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+    bool nv = !gamma_rule && fabsf(spv[J] - thr_v) <= 1e-3f * thr_v;
+    bool ns = !gamma_rule && fabsf(sps[J] - thr_s) <= 1e-3f * thr_s;
+    nv |= pad_v && fabsf(spv[J] - kth_v) <= 1e-3f * kth_v;
+    ns |= pad_s && fabsf(sps[J] - kth_s) <= 1e-3f * kth_s;
+    near += (nv ? 1 : 0) + (ns ? 1 : 0);
+  }
+  near = block_count_1024(near, red);
   for (int J = threadIdx.x; J < nb; J += blockDim.x) {
     a.selv[hb + J] = ssv[J];
     a.sels[hb + J] = sss[J];
   }
   if (threadIdx.x == 0) {
+    a.near[h * 3 + 1] = near;
     a.mu[h * 2] = mu_v;
     a.mu[h * 2 + 1] = mu_s;
     a.counts[h * 4 + 0] = cv;
@@ -678,14 +719,17 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   a.anc = w.anc;
   a.err = w.err;
   a.timeout_ns = ctx->timeout_ns;
-  proxy_tile_stats_kernel<<<dim3(s.H, nchunks), kProxyThreads, kProxySmem, st>>>(tmQ, tmK, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  proxy_row_stats_kernel<<<dim3(kRowSplit, s.H), 256, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb,
-                                                               w.row_part, w.row_ticket, w.rowM,
-                                                               w.rowZ);
-  proxy_pool_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(
-      w.st_m, w.st_u, w.st_w, w.rowM, w.rowZ, s.nb, 1.f / kBlk, w.pv, w.pshi, w.pslo);
+  {
+    PhaseRange range("PatSearch");
+    proxy_tile_stats_kernel<<<dim3(s.H, nchunks), kProxyThreads, kProxySmem, st>>>(tmQ, tmK, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    proxy_row_stats_kernel<<<dim3(kRowSplit, s.H), 256, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb,
+                                                                 w.row_part, w.row_ticket,
+                                                                 w.rowM, w.rowZ);
+    proxy_pool_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(
+        w.st_m, w.st_u, w.st_w, w.rowM, w.rowZ, s.nb, 1.f / kBlk, w.pv, w.pshi, w.pslo);
+  }
   RouteArgs r;
   r.nb = s.nb;
   r.inv_b = 1.f / kBlk;
@@ -708,10 +752,12 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   r.route = w.route;
   r.mu = w.mu;
   r.counts = w.counts;
+  r.near = w.near;
   r.selv = w.selv;
   r.sels = w.sels;
   const size_t dyn = static_cast<size_t>(r.n2) * sizeof(uint64_t) +
                     static_cast<size_t>(s.nb) * (2 * sizeof(float) + 2);
+  PhaseRange range("VS");
   route_vs_select_kernel<<<s.H, 1024, dyn, st>>>(r);
   return cudaGetLastError();
 }
@@ -761,7 +807,8 @@ constexpr size_t kOffPslo = kOffPshi + align256(sizeof(float) * kStaticMaxTiles)
 constexpr size_t kOffPs = kOffPslo + align256(sizeof(float) * kStaticMaxTiles);
 constexpr size_t kOffMu = kOffPs + align256(sizeof(float) * kStaticMaxTiles);
 constexpr size_t kOffCounts = kOffMu + align256(sizeof(float) * kStaticMaxHeads * 2);
-constexpr size_t kOffSelv = kOffCounts + align256(sizeof(int32_t) * kStaticMaxHeads * 4);
+constexpr size_t kOffNear = kOffCounts + align256(sizeof(int32_t) * kStaticMaxHeads * 4);
+constexpr size_t kOffSelv = kOffNear + align256(sizeof(int32_t) * kStaticMaxHeads * 3);
 constexpr size_t kOffSels = kOffSelv + align256(kStaticMaxTiles);
 constexpr size_t kOffPart = kOffSels + align256(kStaticMaxTiles);
 constexpr size_t kOffTicket = kOffPart + align256(sizeof(float2) * kStaticMaxHeads * kRowSplit * kBlk);
@@ -880,6 +927,7 @@ extern "C" crisp_status crisp_route_static(const crisp_dims* dims, const void* Q
   w.ps = reinterpret_cast<float*>(b + kOffPs);
   w.mu = reinterpret_cast<float*>(b + kOffMu);
   w.counts = reinterpret_cast<int32_t*>(b + kOffCounts);
+  w.near = reinterpret_cast<int32_t*>(b + kOffNear);
   w.selv = b + kOffSelv;
   w.sels = b + kOffSels;
   w.row_part = reinterpret_cast<float2*>(b + kOffPart);

@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
                                                       const PeState* __restrict__ pe,
                                                       const int64_t* __restrict__ eq_off,
                                                       int nb, int nbw, uint32_t* rowmask,
-                                                      int32_t* counts) {
+                                                      int32_t* counts, int32_t* near) {
   const int h = blockIdx.y;
   if (route[h]) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -696,6 +696,9 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
   uint32_t* mrow = rowmask + (static_cast<size_t>(h) * nb + I) * nbw;
   const int nw = (I >> 5) + 1;  // words holding keys K <= I
   int selected = 0;
+  // near-threshold pairs: |v - T| <= 1e-3 T (none counted when the whole triangle is kept)
+  const float T = __uint_as_float(st.thresh);
+  int near_cnt = 0;
   for (int wd0 = 0; wd0 < nw; wd0 += 4) {
     uint32_t x[4];
 #pragma unroll
@@ -709,6 +712,7 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
       if (wd >= nw) break;
       const bool valid = wd * 32 + lane <= I;
       bool sel = valid && (all || x[u] > st.thresh);
+      near_cnt += (valid && !all && fabsf(__uint_as_float(x[u]) - T) <= 1e-3f * T) ? 1 : 0;
       if (!all) {
         const bool eq = valid && x[u] == st.thresh;
         if (rank_ties) {
@@ -727,7 +731,10 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
     }
   }
   for (int wd = nw + lane; wd < nbw; wd += 32) mrow[wd] = 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) near_cnt += __shfl_xor_sync(0xffffffffu, near_cnt, o);
   if (lane == 0) {
+    if (near_cnt) atomicAdd(&near[h * 3 + 2], near_cnt);
     atomicAdd(&counts[h * 4 + 0], selected);
     if (selected == 0) atomicAdd(&counts[h * 4 + 1], 1);
   }
@@ -777,7 +784,7 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
                                                                 w.eq_off);
   pe_eqscan_kernel<<<s.H, 1024, 0, st>>>(w.route, w.pe, s.nb, w.eq_off);
   pe_mask_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, w.eq_off, s.nb,
-                                                            s.nbw, w.rowmask, w.counts);
+                                                            s.nbw, w.rowmask, w.counts, w.near);
   return cudaGetLastError();
 }
 

@@ -186,6 +186,16 @@ typedef struct {
   int64_t pe_rescued;  /* PE rows whose only block is the forced diagonal               */
   int32_t n_vs;        /* heads routed VS                                                */
   int32_t n_pe;        /* heads routed PE                                                */
+  /* Near-threshold items, counted on the device: decisions that a relative change of
+   * 1e-3 in the deciding score could flip.  Routes: |C_struct - tau| <= 1e-3 tau.  VS
+   * blocks (both directions of every VS head): |p_d[J] - alpha mu_d| <= 1e-3 alpha mu_d,
+   * or, when the k_min padding applies (or CRISP_FLAG_VS_GAMMA_CUMSUM), within 1e-3 of
+   * the smallest kept score.  PE pairs: |v - v*| <= 1e-3 v*, v* the gamma cut's value
+   * (0 for a head whose cut keeps the whole triangle).  They describe the last
+   * crisp_select (or crisp_prefill); crisp_selection_set leaves them as they were. */
+  int32_t near_routes;
+  int64_t near_vs_blocks;
+  int64_t near_pe_pairs;
 } crisp_stats;
 
 crisp_status crisp_selection_stats(crisp_ctx ctx, const crisp_dims* dims, void* stream,

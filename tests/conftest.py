@@ -24,7 +24,8 @@ def pytest_terminal_summary(terminalreporter):
     keys = ("heads", "vs_heads", "pe_heads", "route_mismatch_exempt", "vs_block_exempt",
             "max_vs_exempt_head", "pe_pair_exempt", "max_pe_exempt_head", "max_p_err",
             "max_cstruct_err", "attend_max_abs", "attend_mean_abs", "attend_rel_rms",
-            "prefill_heads_compared", "prefill_heads_on_gpu_selection")
+            "prefill_heads_compared", "prefill_heads_on_gpu_selection", "near_routes",
+            "near_vs_blocks", "near_pe_pairs")
     terminalreporter.section("parity reports")
     for name, rep in REPORTS:
         parts = []

@@ -193,6 +193,36 @@ def compare_selection(w, sel, osel, heads=None, g=None):
     return rep
 
 
+def near_threshold_counts(w, osel, tol=TOL_REL):
+    """Items of the oracle's selection within `tol` relative of the threshold that decides
+    them -- what crisp_stats' near_* fields count on the device: routes with
+    |C_struct - tau| <= tol tau; VS blocks with |p_d - alpha mu_d| <= tol alpha mu_d (the
+    floor rule) or within tol of the smallest kept score where the k_min padding or the
+    gamma-cumsum rule decided the set; PE pairs with |v - v*| <= tol v* (heads whose cut
+    keeps the whole triangle count none)."""
+    routes = vs = pe = 0
+    gamma_rule = getattr(w, "vs_rule", "floor") == "gamma"
+    for h, o in osel.items():
+        routes += int(abs(o["c_struct"] - w.tau_proxy) <= tol * abs(w.tau_proxy))
+        if o["route_vs"]:
+            for d in ("v", "s"):
+                p = o["p_" + d]
+                near = np.zeros(p.size, bool)
+                if not gamma_rule:
+                    thr = w.alpha * o["mu_" + d]
+                    near |= np.abs(p - thr) <= tol * thr
+                if gamma_rule or o["k_" + d] > o["c_" + d]:
+                    kth = p[o["S_" + d]].min()
+                    near |= np.abs(p - kth) <= tol * kth
+                vs += int(near.sum())
+        else:
+            nb = o["v"].shape[0]
+            if o["n_selected"] < nb * (nb + 1) // 2:
+                tri = o["v"][np.tril_indices(nb)]
+                pe += int((np.abs(tri - o["v_star"]) <= tol * o["v_star"]).sum())
+    return dict(near_routes=routes, near_vs_blocks=vs, near_pe_pairs=pe)
+
+
 def compare_outputs(got, ref, what=""):
     """got, ref: float arrays of the same rows.  Returns (max_abs, mean_abs, rel_rms)."""
     d = np.abs(got.astype(np.float64) - ref)

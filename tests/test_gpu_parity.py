@@ -7,8 +7,9 @@ the oracle's own index set must be within max abs 2e-2 / mean abs 2e-3 (tests/pa
 import numpy as np
 import pytest
 
-from tests.parity import (REPORTS, compare_outputs, compare_selection, csr_from_masks,
-                          gpu_masks, oracle_outputs, oracle_select, to_device)
+from tests.parity import (REPORTS, TOL_REL, compare_outputs, compare_selection,
+                          csr_from_masks, gpu_masks, near_threshold_counts, oracle_outputs,
+                          oracle_select, to_device)
 from workloads import get
 from workloads.configs import Workload
 from workloads.planted import generate, random_qkv
@@ -62,6 +63,15 @@ def run_parity(dsp, w, g, sample=None, seed=0, flags=0, report=None):
         force = "pe"
     osel = oracle_select(w, g) if force is None else _oracle_forced(w, g, force)
     rep = compare_selection(w, sel, osel, g=g)
+    # near-threshold counts made on the device against the oracle's, the band edges widened
+    # by 3% for the scores' own rounding differences
+    dev = ctx.stats(dims)
+    rep.update({k: dev[k] for k in ("near_routes", "near_vs_blocks", "near_pe_pairs")})
+    if w.alpha > 0 and rep["route_mismatch_exempt"] == 0:
+        lo = near_threshold_counts(w, osel, TOL_REL * 0.97)
+        hi = near_threshold_counts(w, osel, TOL_REL * 1.03)
+        for key in lo:
+            assert lo[key] <= dev[key] <= hi[key], (key, dev[key], lo[key], hi[key])
 
     if sample is None:
         blocks = {h: list(range(nb)) for h in range(w.hq)}

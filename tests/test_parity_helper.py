@@ -91,3 +91,15 @@ def test_helper_rejects_pe_row_without_diagonal(tiny):
     sel["row_ptr"], sel["col"] = _with_mask(w, osel, 1, m)
     with pytest.raises(AssertionError):
         P.compare_selection(w, sel, osel, g=g)
+
+
+def test_near_threshold_counts_grow_with_the_band(tiny):
+    """The oracle-side band counts (the reference for crisp_stats' near_* fields) are
+    monotone in the band width and count the diffuse head's ties around its cut value."""
+    w, g, osel = tiny
+    a = P.near_threshold_counts(w, osel, 1e-4)
+    b = P.near_threshold_counts(w, osel)
+    c = P.near_threshold_counts(w, osel, 1e-1)
+    for k in a:
+        assert 0 <= a[k] <= b[k] <= c[k]
+    assert c["near_pe_pairs"] > b["near_pe_pairs"] > 0
