@@ -191,7 +191,7 @@ typedef struct {
    * blocks (both directions of every VS head): |p_d[J] - alpha mu_d| <= 1e-3 alpha mu_d,
    * or, when the k_min padding applies (or CRISP_FLAG_VS_GAMMA_CUMSUM), within 1e-3 of
    * the smallest kept score.  PE pairs: |v - v*| <= 1e-3 v*, v* the gamma cut's value
-   * (0 for a head whose cut keeps the whole triangle).  They describe the last
+   * (0 for a head whose scores sum to less than gamma: the cut then keeps everything).  They describe the last
    * crisp_select (or crisp_prefill); crisp_selection_set leaves them as they were. */
   int32_t near_routes;
   int64_t near_vs_blocks;

@@ -198,8 +198,8 @@ def near_threshold_counts(w, osel, tol=TOL_REL):
     them -- what crisp_stats' near_* fields count on the device: routes with
     |C_struct - tau| <= tol tau; VS blocks with |p_d - alpha mu_d| <= tol alpha mu_d (the
     floor rule) or within tol of the smallest kept score where the k_min padding or the
-    gamma-cumsum rule decided the set; PE pairs with |v - v*| <= tol v* (heads whose cut
-    keeps the whole triangle count none)."""
+    gamma-cumsum rule decided the set; PE pairs with |v - v*| <= tol v* (heads whose scores
+    sum to less than gamma, so that no cut value exists, count none)."""
     routes = vs = pe = 0
     gamma_rule = getattr(w, "vs_rule", "floor") == "gamma"
     for h, o in osel.items():
@@ -217,8 +217,8 @@ def near_threshold_counts(w, osel, tol=TOL_REL):
                 vs += int(near.sum())
         else:
             nb = o["v"].shape[0]
-            if o["n_selected"] < nb * (nb + 1) // 2:
-                tri = o["v"][np.tril_indices(nb)]
+            tri = o["v"][np.tril_indices(nb)]
+            if tri.sum() >= w.gamma:
                 pe += int((np.abs(tri - o["v_star"]) <= tol * o["v_star"]).sum())
     return dict(near_routes=routes, near_vs_blocks=vs, near_pe_pairs=pe)
 

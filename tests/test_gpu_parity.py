@@ -67,7 +67,9 @@ def run_parity(dsp, w, g, sample=None, seed=0, flags=0, report=None):
     # by 3% for the scores' own rounding differences
     dev = ctx.stats(dims)
     rep.update({k: dev[k] for k in ("near_routes", "near_vs_blocks", "near_pe_pairs")})
-    if w.alpha > 0 and rep["route_mismatch_exempt"] == 0:
+    # (alpha = 0 puts the VS threshold at 0, and gamma = 1 leaves it to rounding whether the
+    # PE scores reach gamma at all: both are left out)
+    if w.alpha > 0 and w.gamma < 1 and rep["route_mismatch_exempt"] == 0:
         lo = near_threshold_counts(w, osel, TOL_REL * 0.97)
         hi = near_threshold_counts(w, osel, TOL_REL * 1.03)
         for key in lo:
