@@ -87,6 +87,12 @@ WORKLOADS = {
     "llama8b_n512k": Workload("llama8b_n512k", n=524288, hq=32, hkv=8, seed=1004,
                               sink_scale=4.0, needles=("fixed", 16),
                               pe_heads=_one_pe_per_group(32, 8)),
+    # The first two KV groups of llama8b_n512k (the same heads, bit for bit: every head has
+    # its own seed stream): the 512k layer's per-KV-head attention launches on a case that
+    # holds ~3.5 GB on the device, for counter captures.
+    "llama8b_n512k_kv2": Workload("llama8b_n512k_kv2", n=524288, hq=8, hkv=2, seed=1004,
+                                  sink_scale=4.0, needles=("fixed", 16),
+                                  pe_heads=_one_pe_per_group(8, 2)),
 }
 
 
