@@ -306,7 +306,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.row_ptr), sizeof(int64_t) * (H * nb + 1)},
       {reinterpret_cast<void**>(&w.col), sizeof(int32_t) * w.col_cap},
       {reinterpret_cast<void**>(&w.order), sizeof(int32_t) * H * nb},
-      {reinterpret_cast<void**>(&w.len_hist), sizeof(int32_t) * (Hkv * (nb + 1) + 2)},
+      {reinterpret_cast<void**>(&w.len_hist), sizeof(int32_t) * (Hkv * (nb + 1 + kOrderShortBins) + 2)},
       {reinterpret_cast<void**>(&w.redo), sizeof(int32_t) * H * nb},
       {reinterpret_cast<void**>(&w.redo_count), sizeof(int)},
       {reinterpret_cast<void**>(&w.work_ctr), sizeof(int) * Hkv},

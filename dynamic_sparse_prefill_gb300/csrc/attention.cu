@@ -1007,15 +1007,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Counting sort of the selection's rows by (launch, descending length), a launch being
-// `per` consecutive KV heads: each launch of the fast kernel hands its rows out longest
-// first across all of its KV heads.  Rows with the same key keep no particular order.
+// Counting sort of the selection's rows into the work order of the fast kernel, a launch
+// being `per` consecutive KV heads.  Within a launch: rows longer than kShortRow blocks by
+// exact length, longest first (the long rows of PE heads: each streams its KV head's blocks
+// from the first one up); then the short rows (VS heads) by length class, longest class
+// first, and within a class by band of query blocks, so that rows whose local blocks
+// overlap (neighbouring query blocks, and the query heads that share the KV head) run close
+// together in time and find those blocks in L2.  Rows with the same key keep no particular
+// order.
+constexpr int kShortRow = 64;
+constexpr int kShortClasses = kShortRow / 8;
+constexpr int kBands = 32;
+static_assert(kShortClasses * kBands == kOrderShortBins, "work-order bins of the short rows");
+__host__ __device__ constexpr int order_bins_per_launch(int nb) {
+  return nb + 1 + kShortClasses * kBands;
+}
 __device__ __forceinline__ int order_key(const int64_t* row_ptr, int row, int nb, int hq, int hkv,
                                          int group, int per) {
-  const int h = row / nb;
+  const int h = row / nb, I = row % nb;
   const int hk = (h / hq) * hkv + (h % hq) / group;
   const int len = static_cast<int>(row_ptr[row + 1] - row_ptr[row]);
-  return (hk / per) * (nb + 1) + (nb - len);
+  const int base = (hk / per) * order_bins_per_launch(nb);
+  if (len > kShortRow) return base + (nb - len);
+  const int cls = (max(len, 1) - 1) >> 3;  // 0 .. kShortClasses - 1
+  const int band = static_cast<int>((static_cast<int64_t>(I) * kBands) / nb);
+  return base + (nb + 1) + (kShortClasses - 1 - cls) * kBands + band;
 }
 
 __global__ void order_hist_kernel(const int64_t* __restrict__ row_ptr, int rows, int nb, int hq,
@@ -1093,7 +1109,7 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   if (!dense) {
     PhaseRange range("work order");
     const int rows = s.H * s.nb;
-    const int nbins = nlaunch * (s.nb + 1);
+    const int nbins = nlaunch * order_bins_per_launch(s.nb);
     cudaError_t e = cudaMemsetAsync(ctx->ws.len_hist, 0, sizeof(int) * nbins, st);
     if (e != cudaSuccess) return e;
     order_hist_kernel<<<(rows + 255) / 256, 256, 0, st>>>(ctx->ws.row_ptr, rows, s.nb, s.hq, s.hkv,

@@ -29,7 +29,9 @@ struct PeState {
 
 // CTAs per head that merge PatSearch's per-tile row statistics (patsearch.cu).
 constexpr int kRowSplit = 16;
-
+// Work-order bins of the attention's short rows per launch (length classes x query-block
+// bands, attention.cu); the workspace sizes the order histogram with them.
+constexpr int kOrderShortBins = 256;
 struct Workspace {
   // PatSearch per-tile statistics, [H][nb][128] each (log2 domain max, sums under it)
   float* st_m = nullptr;
@@ -68,7 +70,7 @@ struct Workspace {
   int64_t col_cap = 0;
   // attention work order: rows sorted by descending length (counting sort)
   int32_t* order = nullptr;     // [H*nb]
-  int32_t* len_hist = nullptr;  // [Hkv*(nb+1)] histogram of (KV head, length), then cursors
+  int32_t* len_hist = nullptr;  // [Hkv*(nb+1+kOrderShortBins)] histogram of the work-order keys, then cursors
   // rows the fast attention pass hands to the rescue pass (see attention.cu)
   int32_t* redo = nullptr;      // [H*nb]
   int* redo_count = nullptr;
