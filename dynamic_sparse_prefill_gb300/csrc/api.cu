@@ -293,6 +293,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.near), sizeof(int32_t) * H * 3},
       {reinterpret_cast<void**>(&w.selv), static_cast<size_t>(H * nb)},
       {reinterpret_cast<void**>(&w.sels), static_cast<size_t>(H * nb)},
+      {reinterpret_cast<void**>(&w.selbits), sizeof(uint32_t) * H * (2 * nbw + 1)},
       {reinterpret_cast<void**>(&w.qs), sizeof(uint16_t) * 2 * H * nb * kD},
       {reinterpret_cast<void**>(&w.ks), sizeof(uint16_t) * 2 * Hkv * nb * kD},
       {reinterpret_cast<void**>(&w.kbar), sizeof(float) * Hkv * nb * kD},

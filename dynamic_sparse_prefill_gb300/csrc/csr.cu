@@ -15,32 +15,21 @@ namespace {
 
 constexpr int kRowsPerCta = 32;
 
-// Row masks of a VS head, one 32-key word per thread.  The vertical selection and the
-// slash selection reversed (bit x = sels[N_b-1-x]) are first packed into bit arrays in
-// shared memory; for query block I, key K <= I is a slash key iff sels[I-K], i.e. bit
-// N_b-1-I+K of the reversed array, so a row word is a 64-bit funnel shift of that array.
+// Row masks of a VS head, one 32-key word per thread.  The route kernel wrote the vertical
+// selection and the slash selection reversed (bit x = sels[N_b-1-x]) as bit arrays; for
+// query block I, key K <= I is a slash key iff sels[I-K], i.e. bit N_b-1-I+K of the
+// reversed array, so a row word is a 64-bit funnel shift of that array.
 __global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restrict__ route,
-                                                         const uint8_t* __restrict__ selv,
-                                                         const uint8_t* __restrict__ sels,
+                                                         const uint32_t* __restrict__ selbits,
                                                          int nb, int nbw, uint32_t* rowmask) {
   extern __shared__ uint32_t sbits[];  // [nbw] vertical, [nbw + 1] reversed slash
   const int h = blockIdx.y;
   if (!route[h]) return;
-  uint32_t* sv = sbits;
-  uint32_t* sr = sbits + nbw;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint8_t* v = selv + static_cast<size_t>(h) * nb;
-  const uint8_t* sl = sels + static_cast<size_t>(h) * nb;
-  for (int wd = warp; wd <= nbw; wd += 8) {
-    const int x = wd * 32 + lane;
-    const unsigned wv = __ballot_sync(0xffffffffu, wd < nbw && x < nb && v[x] != 0);
-    const unsigned ws = __ballot_sync(0xffffffffu, x < nb && sl[nb - 1 - x] != 0);
-    if (lane == 0) {
-      if (wd < nbw) sv[wd] = wv;
-      sr[wd] = ws;
-    }
-  }
+  const uint32_t* src = selbits + static_cast<size_t>(h) * (2 * nbw + 1);
+  for (int i = threadIdx.x; i < 2 * nbw + 1; i += blockDim.x) sbits[i] = src[i];
   __syncthreads();
+  const uint32_t* sv = sbits;
+  const uint32_t* sr = sbits + nbw;
   const int I0 = blockIdx.x * kRowsPerCta;
   const int nrows = min(kRowsPerCta, nb - I0);
   for (int idx = threadIdx.x; idx < nrows * nbw; idx += blockDim.x) {
@@ -183,8 +172,8 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st) {
   Workspace& w = ctx->ws;
   vs_rowmask_kernel<<<dim3((s.nb + kRowsPerCta - 1) / kRowsPerCta, s.H), 256,
-                      sizeof(uint32_t) * (2 * s.nbw + 1), st>>>(w.route, w.selv, w.sels, s.nb,
-                                                                 s.nbw, w.rowmask);
+                      sizeof(uint32_t) * (2 * s.nbw + 1), st>>>(w.route, w.selbits, s.nb, s.nbw,
+                                                                 w.rowmask);
   const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
   const int nblk = static_cast<int>((rows + 1023) / 1024);
   csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.rowmask, rows, s.nbw, w.row_ptr, w.scan_blk);

@@ -53,6 +53,9 @@ struct Workspace {
   int32_t* near = nullptr;   // [H][3] near-threshold route, VS blocks, PE pairs (crisp_stats)
   uint8_t* selv = nullptr;   // [H][nb]
   uint8_t* sels = nullptr;   // [H][nb]
+  // VS heads: S_v as bits (bit x of word x/32 = block x), then S_s reversed as bits
+  // (bit x = slash block N_b-1-x, one spare word), [H][2*nbw+1] (patsearch.cu -> csr.cu)
+  uint32_t* selbits = nullptr;
   // PEIndex
   uint16_t* qs = nullptr;    // [2][H*nb][128] bf16: Qbar * log2(e)/sqrt(d) as hi rows, then lo rows
   uint16_t* ks = nullptr;    // [2][Hkv*nb][128] bf16: Kbar as hi rows, then lo rows

@@ -387,6 +387,7 @@ struct RouteArgs {
   int32_t* near;  // [H][3]: near-threshold route, VS blocks, (PE pairs: pe_index.cu)
   uint8_t* selv;
   uint8_t* sels;
+  uint32_t* selbits;  // [H][2*nbw+1] (may be null: crisp_route_static)
 };
 
 __device__ float block_sum_1024(float x, float* red) {
@@ -671,6 +672,22 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
     a.selv[hb + J] = ssv[J];
     a.sels[hb + J] = sss[J];
   }
+  // The two sets as bit words for the row masks (csr.cu): S_v in block order, S_s reversed
+  // (bit x = slash block N_b-1-x), so that a row's slash keys are one funnel shift.
+  if (a.selbits) {
+    const int nbw = (nb + 31) / 32;
+    uint32_t* out = a.selbits + static_cast<size_t>(h) * (2 * nbw + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int wd = warp; wd <= nbw; wd += blockDim.x >> 5) {
+      const int x = wd * 32 + lane;
+      const unsigned wv = __ballot_sync(0xffffffffu, wd < nbw && x < nb && ssv[x] != 0);
+      const unsigned ws = __ballot_sync(0xffffffffu, x < nb && sss[nb - 1 - x] != 0);
+      if (lane == 0) {
+        if (wd < nbw) out[wd] = wv;
+        out[nbw + wd] = ws;
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     a.near[h * 3 + 1] = near;
     a.mu[h * 2] = mu_v;
@@ -755,6 +772,7 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   r.near = w.near;
   r.selv = w.selv;
   r.sels = w.sels;
+  r.selbits = w.selbits;
   const size_t dyn = static_cast<size_t>(r.n2) * sizeof(uint64_t) +
                     static_cast<size_t>(s.nb) * (2 * sizeof(float) + 2);
   PhaseRange range("VS");

@@ -20,7 +20,7 @@ def L():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "crisp.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(crisp_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(crisp_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(L):
