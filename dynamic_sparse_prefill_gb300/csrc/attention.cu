@@ -1070,7 +1070,54 @@ __global__ void order_scatter_kernel(const int64_t* __restrict__ row_ptr, int ro
     order[atomicAdd(&cursor[order_key(row_ptr, row, nb, hq, hkv, group, per)], 1)] = row;
 }
 
+// The same counting sort in one CTA for short sequences (rows <= kOrderSmallRows and the
+// histogram in shared memory): one launch instead of a memset and three.
+constexpr int kOrderSmallRows = 16384;
+constexpr int kOrderSmallBins = 12288;
+__global__ void __launch_bounds__(1024) order_small_kernel(const int64_t* __restrict__ row_ptr,
+                                                           int rows, int nb, int hq, int hkv,
+                                                           int group, int per, int nbins,
+                                                           int32_t* order) {
+  extern __shared__ int hist[];  // [nbins]
+  __shared__ int part[1024];
+  for (int i = threadIdx.x; i < nbins; i += 1024) hist[i] = 0;
+  __syncthreads();
+  for (int row = threadIdx.x; row < rows; row += 1024)
+    atomicAdd(&hist[order_key(row_ptr, row, nb, hq, hkv, group, per)], 1);
+  __syncthreads();
+  const int pc = (nbins + 1023) / 1024;
+  const int p0 = threadIdx.x * pc, p1 = min(nbins, p0 + pc);
+  int s = 0;
+  for (int p = p0; p < p1; ++p) s += hist[p];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int t = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += t;
+    __syncthreads();
+  }
+  int run = part[threadIdx.x] - s;
+  for (int p = p0; p < p1; ++p) {
+    const int c = hist[p];
+    hist[p] = run;
+    run += c;
+  }
+  __syncthreads();
+  for (int row = threadIdx.x; row < rows; row += 1024)
+    order[atomicAdd(&hist[order_key(row_ptr, row, nb, hq, hkv, group, per)], 1)] = row;
+}
+
 }  // namespace
+
+// Launches of the attention work order for these shapes (1 or 3).
+int order_launches(const Shape& s, int num_sms) {
+  const int per = attention_kv_heads_per_launch(s, num_sms);
+  const int nlaunch = (s.Hkv + per - 1) / per;
+  const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
+  const int64_t nbins = static_cast<int64_t>(nlaunch) * order_bins_per_launch(s.nb);
+  return rows <= kOrderSmallRows && nbins <= kOrderSmallBins ? 1 : 3;
+}
 
 // KV heads per launch of the fast kernel: enough rows for 8 per SM, and beyond that as many
 // KV heads as keep their K and V (2 x n x 128 x 2 bytes each) within 48 MB of L2, so that
@@ -1106,7 +1153,14 @@ cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& t
   const int per_kv = s.group * s.nb;
   const int per = attention_kv_heads_per_launch(s, ctx->num_sms);
   const int nlaunch = (s.Hkv + per - 1) / per;
-  if (!dense) {
+  if (!dense && order_launches(s, ctx->num_sms) == 1) {
+    PhaseRange range("work order");
+    const int rows = s.H * s.nb;
+    const int nbins = nlaunch * order_bins_per_launch(s.nb);
+    order_small_kernel<<<1, 1024, sizeof(int) * nbins, st>>>(ctx->ws.row_ptr, rows, s.nb, s.hq,
+                                                             s.hkv, s.group, per, nbins,
+                                                             ctx->ws.order);
+  } else if (!dense) {
     PhaseRange range("work order");
     const int rows = s.H * s.nb;
     const int nbins = nlaunch * order_bins_per_launch(s.nb);

@@ -171,8 +171,14 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
                             const void* K, const CUtensorMap& tmQs, const CUtensorMap& tmKs,
                             const CUtensorMap& tmO, bool tma_out, cudaStream_t st);
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st);
+// Launches of PatSearch and the route (2 for short sequences, else 4).
+int patsearch_launches(int nb);
+// Launches of the PE gamma cut after the pooled softmax (1 for short sequences, else 12).
+int pe_select_launches(int nb);
 // KV heads per launch of the fast attention kernel (launch_attention splits the heads).
 int attention_kv_heads_per_launch(const Shape& s, int num_sms);
+// Launches of the attention work order (1 for short sequences, else 3).
+int order_launches(const Shape& s, int num_sms);
 // tmQ/tmK/tmV: 3-D maps of Q, K, V (dims {64, rows, 2}, box {64, 128, 2}; see make_map3).
 cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& tmQ,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, void* O, bool dense,

@@ -368,6 +368,11 @@ __global__ void __launch_bounds__(256) proxy_pool_kernel(
 
 struct RouteArgs {
   int nb;
+  // 1: this kernel also merges the per-tile statistics into the row maxima and sums and
+  // pools them by tile (what proxy_row_stats and proxy_pool do), for N_b <= kFuseRowsNb
+  int fuse_rows;
+  const float* st_u;
+  const float* st_w;
   int n2;  // power of two >= nb (sort width)
   float inv_b, tau, alpha, gamma;
   int kmin_blocks;
@@ -376,7 +381,7 @@ struct RouteArgs {
   const float* anc;
   const float* rowM;
   const float* rowZ;
-  const float* pv;
+  float* pv;  // read, or written by this kernel when fuse_rows
   const float* pshi;
   const float* pslo;
   float* ps;
@@ -564,6 +569,10 @@ __device__ void select_gamma_cumsum(const float* p, uint8_t* sel, int nb, float 
   *out_k = k;
 }
 
+// Short sequences: the route kernel merges the per-tile statistics itself (one launch
+// instead of three); the same formulas as proxy_row_stats and proxy_pool.
+constexpr int kFuseRowsNb = 256;
+
 __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a) {
   extern __shared__ uint64_t sdyn64[];
   uint64_t* keys = sdyn64;                                  // [n2]
@@ -575,16 +584,88 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
   __shared__ float redf[32];
   __shared__ double part[1024];
   __shared__ int first;
+  __shared__ float sRowM[kBlk], sRowZ[kBlk];
   const int h = blockIdx.x;
   const int nb = a.nb;
   const size_t hb = static_cast<size_t>(h) * nb;
+
+  if (a.fuse_rows) {
+    // Row maximum and normaliser of every proxy row over all tiles (8 slices of tiles
+    // merged online, then the slices), then the pooled contributions of every tile.
+    float* pM = reinterpret_cast<float*>(part);  // [8][128] (part's bytes, unused yet)
+    float* pZ = pM + 8 * kBlk;
+    const int r = threadIdx.x & (kBlk - 1), slice = threadIdx.x >> 7;
+    float M = -FLT_MAX, Z = 0.f;
+    for (int t = slice; t < nb; t += 8) {
+      const size_t idx = (hb + t) * kBlk + r;
+      const float m = a.st_m[idx];
+      const float sum = a.st_u[idx] + a.st_w[idx];
+      if (m > M) {
+        Z = Z * fast_exp2(M - m) + sum;
+        M = m;
+      } else {
+        Z += sum * fast_exp2(m - M);
+      }
+    }
+    pM[slice * kBlk + r] = M;
+    pZ[slice * kBlk + r] = Z;
+    __syncthreads();
+    if (threadIdx.x < kBlk) {
+      float Mt = -FLT_MAX;
+      for (int i = 0; i < 8; ++i) Mt = fmaxf(Mt, pM[i * kBlk + r]);
+      float Zt = 0.f;
+      for (int i = 0; i < 8; ++i) Zt += pZ[i * kBlk + r] * fast_exp2(pM[i * kBlk + r] - Mt);
+      sRowM[r] = Mt;
+      sRowZ[r] = Zt;
+    }
+    __syncthreads();
+    float* shi = spv;  // p_v in spv; the slash halves of each tile in sps and keys' bytes
+    float* slo = reinterpret_cast<float*>(keys);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < nb; t += 32) {
+      float su = 0.f, sw = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = lane + 32 * k;
+        const size_t idx = (hb + t) * kBlk + rr;
+        const float e = fast_exp2(a.st_m[idx] - sRowM[rr]) / sRowZ[rr];
+        su += a.st_u[idx] * e;
+        sw += a.st_w[idx] * e;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        su += __shfl_xor_sync(0xffffffffu, su, o);
+        sw += __shfl_xor_sync(0xffffffffu, sw, o);
+      }
+      if (lane == 0) {
+        a.pv[hb + t] = (su + sw) * a.inv_b;
+        sps[t] = su * a.inv_b;
+        slo[t] = sw * a.inv_b;
+      }
+    }
+    __syncthreads();
+    // p_v[J] = tile J's vertical mass; p_s[J] = hi part of tile N_b-1-J + lo part of N_b-2-J
+    for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+      float s = sps[nb - 1 - J];
+      if (J <= nb - 2) s += slo[nb - 2 - J];
+      shi[J] = s;  // parked in spv until sps is free
+    }
+    __syncthreads();
+    for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+      sps[J] = shi[J];
+      a.ps[hb + J] = shi[J];
+    }
+    __syncthreads();
+    for (int J = threadIdx.x; J < nb; J += blockDim.x) spv[J] = a.pv[hb + J];
+    __syncthreads();
+  }
 
   // C_struct = (1/b) sum_r (anchor mass of row r) -- "Core method" step 1, Algorithm 2.
   float c = 0.f;
   if (threadIdx.x < kBlk) {
     const int r = threadIdx.x;
-    const float M = a.rowM[h * kBlk + r];
-    const float iz = 1.f / a.rowZ[h * kBlk + r];
+    const float M = a.fuse_rows ? sRowM[r] : a.rowM[h * kBlk + r];
+    const float iz = 1.f / (a.fuse_rows ? sRowZ[r] : a.rowZ[h * kBlk + r]);
     c = a.anc[(static_cast<size_t>(h) * 2) * kBlk + r] *
         fast_exp2(a.st_m[hb * kBlk + r] - M);
     if (nb > 1)
@@ -598,12 +679,14 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
   if (a.flags & CRISP_FLAG_FORCE_PE) vs = false;
 
   // p_v[J] = tile J's vertical mass; p_s[J] = hi part of tile N_b-1-J + lo part of N_b-2-J.
-  for (int J = threadIdx.x; J < nb; J += blockDim.x) {
-    spv[J] = a.pv[hb + J];
-    float s = a.pshi[hb + (nb - 1 - J)];
-    if (J <= nb - 2) s += a.pslo[hb + (nb - 2 - J)];
-    sps[J] = s;
-    a.ps[hb + J] = s;
+  if (!a.fuse_rows) {
+    for (int J = threadIdx.x; J < nb; J += blockDim.x) {
+      spv[J] = a.pv[hb + J];
+      float s = a.pshi[hb + (nb - 1 - J)];
+      if (J <= nb - 2) s += a.pslo[hb + (nb - 2 - J)];
+      sps[J] = s;
+      a.ps[hb + J] = s;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -736,19 +819,25 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   a.anc = w.anc;
   a.err = w.err;
   a.timeout_ns = ctx->timeout_ns;
+  const bool fuse = s.nb <= kFuseRowsNb;
   {
     PhaseRange range("PatSearch");
     proxy_tile_stats_kernel<<<dim3(s.H, nchunks), kProxyThreads, kProxySmem, st>>>(tmQ, tmK, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    proxy_row_stats_kernel<<<dim3(kRowSplit, s.H), 256, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb,
-                                                                 w.row_part, w.row_ticket,
-                                                                 w.rowM, w.rowZ);
-    proxy_pool_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(
-        w.st_m, w.st_u, w.st_w, w.rowM, w.rowZ, s.nb, 1.f / kBlk, w.pv, w.pshi, w.pslo);
+    if (!fuse) {
+      proxy_row_stats_kernel<<<dim3(kRowSplit, s.H), 256, 0, st>>>(w.st_m, w.st_u, w.st_w, s.nb,
+                                                                   w.row_part, w.row_ticket,
+                                                                   w.rowM, w.rowZ);
+      proxy_pool_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(
+          w.st_m, w.st_u, w.st_w, w.rowM, w.rowZ, s.nb, 1.f / kBlk, w.pv, w.pshi, w.pslo);
+    }
   }
   RouteArgs r;
   r.nb = s.nb;
+  r.fuse_rows = fuse ? 1 : 0;
+  r.st_u = w.st_u;
+  r.st_w = w.st_w;
   r.inv_b = 1.f / kBlk;
   r.tau = cfg.tau_proxy;
   r.alpha = cfg.alpha;
@@ -779,6 +868,8 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   route_vs_select_kernel<<<s.H, 1024, dyn, st>>>(r);
   return cudaGetLastError();
 }
+
+int patsearch_launches(int nb) { return nb <= kFuseRowsNb ? 2 : 4; }
 
 cudaError_t init_patsearch_attributes() {
   cudaError_t e = cudaFuncSetAttribute(proxy_tile_stats_kernel,

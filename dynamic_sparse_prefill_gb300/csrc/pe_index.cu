@@ -38,21 +38,36 @@ __device__ __forceinline__ void split_store(uint16_t* hi_plane, size_t lo_offset
   hi_plane[lo_offset + idx] = __bfloat16_as_ushort(lo);
 }
 
-// Qbar[h][I][:] = mean of the 128 rows of query block I (PE heads only), times
-// log2(e)/sqrt(d), split into bf16 pairs.
-__global__ void __launch_bounds__(128) pe_pool_q_kernel(const uint16_t* __restrict__ Q,
-                                                        const uint8_t* __restrict__ route,
-                                                        int n, int nb, int H, float scale,
-                                                        uint16_t* qs) {
-  const int h = blockIdx.y, I = blockIdx.x;
-  if (route[h]) return;
+// Block means of the PE heads' queries and of the KV heads that serve them, one launch:
+// grid (H + Hkv, N_b) (heads on x: H + Hkv may pass the 65535 limit of y).  y < H: Qbar[y][I][:] = mean of the 128 rows of query block I of a
+// PE head, times log2(e)/sqrt(d); y >= H: Kbar[y-H][I][:] for a KV head with at least one
+// PE query head.  Both are split into bf16 pairs.
+__global__ void __launch_bounds__(128) pe_pool_kernel(const uint16_t* __restrict__ Q,
+                                                      const uint16_t* __restrict__ K,
+                                                      const uint8_t* __restrict__ route, int n,
+                                                      int nb, int H, int hq, int hkv, int group,
+                                                      int Hkv, float q_scale, uint16_t* qs,
+                                                      uint16_t* ks) {
+  const int y = blockIdx.x, I = blockIdx.y;
+  const bool is_q = y < H;
+  const uint16_t* src;
+  if (is_q) {
+    if (route[y]) return;
+    src = Q + (static_cast<size_t>(y) * n + static_cast<size_t>(I) * kBlk) * kD;
+  } else {
+    const int hk = y - H;
+    const int bidx = hk / hkv, kvh = hk % hkv;
+    bool any_pe = false;
+    for (int g = 0; g < group; ++g) any_pe |= route[bidx * hq + kvh * group + g] == 0;
+    if (!any_pe) return;
+    src = K + (static_cast<size_t>(hk) * n + static_cast<size_t>(I) * kBlk) * kD;
+  }
   __shared__ float part[8][kD];
   const int rg = threadIdx.x >> 4;          // row group 0..7
   const int cc = (threadIdx.x & 15) * 8;    // 8 columns
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const uint16_t* base = Q + (static_cast<size_t>(h) * n + static_cast<size_t>(I) * kBlk) * kD;
   for (int rr = rg; rr < kBlk; rr += 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(rr) * kD + cc);
+    const uint4 v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(rr) * kD + cc);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -66,42 +81,12 @@ __global__ void __launch_bounds__(128) pe_pool_q_kernel(const uint16_t* __restri
   float s = 0.f;
 #pragma unroll
   for (int g = 0; g < 8; ++g) s += part[g][threadIdx.x];
-  split_store(qs, static_cast<size_t>(H) * nb * kD,
-              (static_cast<size_t>(h) * nb + I) * kD + threadIdx.x, s * (1.f / kBlk) * scale);
-}
-
-// Kbar for every KV head that serves at least one PE query head, split into bf16 pairs.
-__global__ void __launch_bounds__(128) pe_pool_k_kernel(const uint16_t* __restrict__ K,
-                                                        const uint8_t* __restrict__ route,
-                                                        int n, int nb, int hq, int hkv,
-                                                        int group, int Hkv, uint16_t* ks) {
-  const int hk = blockIdx.y, I = blockIdx.x;
-  const int bidx = hk / hkv, kvh = hk % hkv;
-  bool any_pe = false;
-  for (int g = 0; g < group; ++g) any_pe |= route[bidx * hq + kvh * group + g] == 0;
-  if (!any_pe) return;
-  __shared__ float part[8][kD];
-  const int rg = threadIdx.x >> 4;
-  const int cc = (threadIdx.x & 15) * 8;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const uint16_t* base = K + (static_cast<size_t>(hk) * n + static_cast<size_t>(I) * kBlk) * kD;
-  for (int rr = rg; rr < kBlk; rr += 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(rr) * kD + cc);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc[2 * k] += __uint_as_float(w[k] << 16);
-      acc[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) part[rg][cc + k] = acc[k];
-  __syncthreads();
-  float s = 0.f;
-#pragma unroll
-  for (int g = 0; g < 8; ++g) s += part[g][threadIdx.x];
-  split_store(ks, static_cast<size_t>(Hkv) * nb * kD,
-              (static_cast<size_t>(hk) * nb + I) * kD + threadIdx.x, s * (1.f / kBlk));
+  if (is_q)
+    split_store(qs, static_cast<size_t>(H) * nb * kD,
+                (static_cast<size_t>(y) * nb + I) * kD + threadIdx.x, s * (1.f / kBlk) * q_scale);
+  else
+    split_store(ks, static_cast<size_t>(Hkv) * nb * kD,
+                (static_cast<size_t>(y - H) * nb + I) * kD + threadIdx.x, s * (1.f / kBlk));
 }
 
 // ---------------------------------------------------------------- pooled softmax
@@ -740,12 +725,295 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
   }
 }
 
+// ---------------------------------------------------------------- short sequences
+// N_b <= kSmallNb: the whole gamma cut of a PE head in one CTA, the triangle held in shared
+// memory (flattened row by row: pair (I, K) at I (I + 1) / 2 + K, the flat order of the
+// cut's ties).  Same steps and rules as the multi-kernel path above: four 8-bit radix
+// passes with fp64 bin masses and the same digit pick, flat-order tie ranks when only some
+// of the items equal to the threshold are taken, then the row masks (plus the diagonal),
+// the kept-pair and rescued-row counts and the near-threshold count.  One launch instead
+// of twelve, which matters at short lengths, where each launch costs about as much as its
+// work.
+constexpr int kSmallNb = 256;
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallCopies = 8;  // shared histogram copies (one per 4 warps)
+
+__host__ __device__ constexpr size_t small_select_smem(int nb) {
+  // flattened triangle (fp32 bits), then the kept-pair bit array with one spare word
+  return (static_cast<size_t>(nb) * (nb + 1) / 2 + (static_cast<size_t>(nb) * (nb + 1) / 2 + 31) / 32 + 2) *
+         sizeof(uint32_t);
+}
+
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    pe_select_small_kernel(const float* __restrict__ pev, const uint8_t* __restrict__ route,
+                           int nb, int nbw, float gamma, uint32_t* rowmask, int32_t* counts,
+                           int32_t* near) {
+  const int h = blockIdx.x;
+  if (route[h]) return;
+  extern __shared__ uint32_t s_dyn[];
+  const int T = nb * (nb + 1) / 2;
+  uint32_t* sv = s_dyn;                  // [T]
+  uint32_t* sbits = s_dyn + T;           // [ceil(T / 32) + 2]
+  __shared__ uint32_t scnt[kSmallCopies][256];
+  __shared__ float smass[kSmallCopies][256];
+  __shared__ int s_red[32];
+  __shared__ PeState s_st;
+  __shared__ int s_sel_total, s_rescued;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // 1. the triangle into shared memory, a warp per row
+  for (int I = warp; I < nb; I += kSmallThreads / 32) {
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(pev + (static_cast<size_t>(h) * nb + I) * nb);
+    uint32_t* dst = sv + I * (I + 1) / 2;
+    for (int K = lane; K <= I; K += 32) dst[K] = row[K];
+  }
+  const int nwords = (T + 31) / 32 + 2;
+  for (int i = tid; i < nwords; i += kSmallThreads) sbits[i] = 0u;
+  if (tid == 0) {
+    PeState z{};
+    s_st = z;
+    s_sel_total = 0;
+    s_rescued = 0;
+  }
+  __syncthreads();
+
+  // 2. four radix passes over the fp32 bit patterns (positive values: bits order like values)
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < kSmallCopies * 256; i += kSmallThreads) {
+      (&scnt[0][0])[i] = 0u;
+      (&smass[0][0])[i] = 0.f;
+    }
+    __syncthreads();
+    const PeState st = s_st;
+    if (st.select_all) break;  // uniform: every thread read the same state
+    const int copy = warp & (kSmallCopies - 1);
+    // Values of a head crowd into few bins (the high digits above all), so a warp whose
+    // matching lanes share a bin adds once (lane count, shuffle-summed mass); otherwise each
+    // lane adds its own value.
+    for (int i0 = 0; i0 < T; i0 += kSmallThreads) {
+      const int i = i0 + tid;
+      const uint32_t bits = i < T ? sv[i] : 0u;
+      const bool match = i < T && (bits & st.decided) == st.prefix;
+      const uint32_t bin = (bits >> shift) & 255u;
+      const unsigned m = __ballot_sync(0xffffffffu, match);
+      if (m == 0) continue;
+      const uint32_t b0 = __shfl_sync(0xffffffffu, bin, __ffs(m) - 1);
+      if (__all_sync(0xffffffffu, !match || bin == b0)) {
+        float x = match ? __uint_as_float(bits) : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) {
+          atomicAdd(&scnt[copy][b0], static_cast<uint32_t>(__popc(m)));
+          atomicAdd(&smass[copy][b0], x);
+        }
+      } else if (match) {
+        atomicAdd(&scnt[copy][bin], 1u);
+        atomicAdd(&smass[copy][bin], __uint_as_float(bits));
+      }
+    }
+    __syncthreads();
+    // the copies combined per bin (count, fp32 mass) before the fp64 pick
+    if (tid < 256) {
+      uint32_t cc = 0;
+      float mm = 0.f;
+#pragma unroll
+      for (int k = 0; k < kSmallCopies; ++k) {
+        cc += scnt[k][tid];
+        mm += smass[k][tid];
+      }
+      scnt[0][tid] = cc;
+      smass[0][tid] = mm;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // the digit whose bin crosses the remaining target, bins walked from the top: lane l
+      // holds bins 255 - 8l .. 248 - 8l (the same pick as pe_digit_kernel)
+      const double rem = static_cast<double>(gamma) - st.mass_above;
+      unsigned long long c[8];
+      double m[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int bin = 255 - (lane * 8 + i);
+        c[i] = scnt[0][bin];
+        m[i] = static_cast<double>(smass[0][bin]);
+      }
+      double local = 0.0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c[i]) local += m[i];
+      double incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      double cum = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) cum = 0.0;
+      int cand = -1, low = -1;
+      double cand_cum = 0.0, low_m = 0.0;
+      unsigned long long cand_c = 0, low_c = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (!c[i]) continue;
+        const int bin = 255 - (lane * 8 + i);
+        if (cand < 0) {
+          if (cum + m[i] >= rem) {
+            cand = bin;
+            cand_cum = cum;
+            cand_c = c[i];
+          } else {
+            cum += m[i];
+          }
+        }
+        low = bin;
+        low_m = m[i];
+        low_c = c[i];
+      }
+      int chosen = -1;
+      double above = 0.0;
+      unsigned long long chosen_c = 0;
+      bool all = false;
+      const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        chosen = __shfl_sync(0xffffffffu, cand, src);
+        above = __shfl_sync(0xffffffffu, cand_cum, src);
+        chosen_c = __shfl_sync(0xffffffffu, cand_c, src);
+      } else {
+        const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
+        const double total = __shfl_sync(0xffffffffu, incl, 31);
+        if (pass == 0 || any == 0) {
+          all = true;  // the whole triangle holds less than gamma
+        } else {
+          const int src = 31 - __clz(any);
+          chosen = __shfl_sync(0xffffffffu, low, src);
+          above = total - __shfl_sync(0xffffffffu, low_m, src);
+          chosen_c = __shfl_sync(0xffffffffu, low_c, src);
+        }
+      }
+      if (lane == 0) {
+        PeState ns = st;
+        if (all) {
+          ns.select_all = 1;
+        } else {
+          ns.mass_above += above;
+          ns.prefix |= static_cast<uint32_t>(chosen) << shift;
+          ns.decided |= 255u << shift;
+          if (pass == 3) {
+            ns.thresh = ns.prefix;
+            ns.count_eq = chosen_c;
+            const double vt = static_cast<double>(__uint_as_float(ns.thresh));
+            const double rem2 = static_cast<double>(gamma) - ns.mass_above;
+            unsigned long long need = ns.count_eq;
+            if (vt > 0.0) {
+              const double q = ceil(rem2 / vt);
+              need = q < 1.0 ? 1ull : static_cast<unsigned long long>(q);
+            }
+            ns.need_eq = need < ns.count_eq ? need : ns.count_eq;
+          }
+        }
+        s_st = ns;
+      }
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  const PeState st = s_st;
+  const bool all = st.select_all != 0;
+  const bool rank_ties = !all && st.need_eq < st.count_eq;
+  const float Tv = __uint_as_float(st.thresh);
+
+  // 3. kept pairs as bits in flat order; every thread owns whole 32-pair words of a
+  // contiguous range (flat-order tie ranks by a scan of the per-thread tie counts)
+  const int words = (T + 31) / 32;
+  const int wper = (words + kSmallThreads - 1) / kSmallThreads;
+  const int f0 = min(T, tid * wper * 32), f1 = min(T, (tid + 1) * wper * 32);
+  int eq = 0;
+  if (rank_ties)
+    for (int f = f0; f < f1; ++f) eq += sv[f] == st.thresh ? 1 : 0;
+  // exclusive scan of eq over the threads
+  int incl = eq;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_red[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_red[lane] = w;
+  }
+  __syncthreads();
+  long long rank = (warp > 0 ? s_red[warp - 1] : 0) + incl - eq;
+  int near_cnt = 0;
+  for (int f = f0; f < f1; f += 32) {
+    uint32_t word = 0;
+    for (int k = 0; k < 32 && f + k < f1; ++k) {
+      const uint32_t bits = sv[f + k];
+      bool sel = all || bits > st.thresh;
+      if (!all && bits == st.thresh) {
+        sel = rank_ties ? rank < static_cast<long long>(st.need_eq) : true;
+        ++rank;
+      }
+      if (!all && fabsf(__uint_as_float(bits) - Tv) <= 1e-3f * Tv) ++near_cnt;
+      if (sel) word |= 1u << k;
+    }
+    sbits[f >> 5] = word;
+  }
+  __syncthreads();
+
+  // 4. row masks (a warp per row: lane = 32-key word), kept-pair and rescued-row counts
+  for (int I = warp; I < nb; I += kSmallThreads / 32) {
+    const int base = I * (I + 1) / 2;
+    int selected = 0;
+    for (int wd0 = 0; wd0 < nbw; wd0 += 32) {
+      const int wd = wd0 + lane;
+      uint32_t word = 0;
+      if (wd < nbw && wd * 32 <= I) {
+        const int o = base + wd * 32;
+        word = __funnelshift_r(sbits[o >> 5], sbits[(o >> 5) + 1], o & 31);
+        const int top = I - wd * 32;  // keys 0..top of this word are in the row
+        if (top < 31) word &= (2u << top) - 1u;
+        selected += __popc(word);
+        if (top < 32) word |= 1u << top;  // the diagonal
+      }
+      if (wd < nbw) rowmask[(static_cast<size_t>(h) * nb + I) * nbw + wd] = word;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) selected += __shfl_xor_sync(0xffffffffu, selected, o);
+    if (lane == 0) {
+      atomicAdd(&s_sel_total, selected);
+      if (selected == 0) atomicAdd(&s_rescued, 1);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) near_cnt += __shfl_xor_sync(0xffffffffu, near_cnt, o);
+  if (lane == 0 && near_cnt) atomicAdd(&near[h * 3 + 2], near_cnt);
+  __syncthreads();
+  if (tid == 0) {
+    counts[h * 4 + 0] = s_sel_total;
+    counts[h * 4 + 1] = s_rescued;
+  }
+}
+
 }  // namespace
 
 cudaError_t init_pe_attributes() {
-  return cudaFuncSetAttribute(pe_prob_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kPeSmem));
+  cudaError_t e = cudaFuncSetAttribute(pe_prob_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kPeSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(pe_select_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(small_select_smem(kSmallNb)));
 }
+
+int pe_select_launches(int nb) { return nb <= kSmallNb ? 1 : 12; }
 
 cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg, const void* Q,
                             const void* K, const CUtensorMap& tmQs, const CUtensorMap& tmKs,
@@ -753,10 +1021,9 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
   Workspace& w = ctx->ws;
   const uint16_t* q = static_cast<const uint16_t*>(Q);
   const uint16_t* k = static_cast<const uint16_t*>(K);
-  pe_pool_q_kernel<<<dim3(s.nb, s.H), 128, 0, st>>>(
-      q, w.route, s.n, s.nb, s.H, 1.4426950408889634f / sqrtf(static_cast<float>(kD)), w.qs);
-  pe_pool_k_kernel<<<dim3(s.nb, s.Hkv), 128, 0, st>>>(k, w.route, s.n, s.nb, s.hq, s.hkv,
-                                                       s.group, s.Hkv, w.ks);
+  pe_pool_kernel<<<dim3(s.H + s.Hkv, s.nb), 128, 0, st>>>(
+      q, k, w.route, s.n, s.nb, s.H, s.hq, s.hkv, s.group, s.Hkv,
+      1.4426950408889634f / sqrtf(static_cast<float>(kD)), w.qs, w.ks);
   PeProbArgs pa;
   pa.route = w.route;
   pa.nb = s.nb;
@@ -772,6 +1039,11 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
   pa.timeout_ns = ctx->timeout_ns;
   pa.tma_out = tma_out ? 1 : 0;
   pe_prob_kernel<<<dim3(s.H, pa.nt), kPeThreads, kPeSmem, st>>>(tmQs, tmKs, tmO, pa);
+  if (s.nb <= kSmallNb) {
+    pe_select_small_kernel<<<s.H, kSmallThreads, small_select_smem(s.nb), st>>>(
+        w.pev, w.route, s.nb, s.nbw, cfg.gamma, w.rowmask, w.counts, w.near);
+    return cudaGetLastError();
+  }
   pe_radix_init_kernel<<<s.H, 256, 0, st>>>(w.pe, w.hist_cnt, w.hist_mass);
   for (int pass = 0; pass < 4; ++pass) {
     const int rpc = hist_rows_per_cta(s.nb);

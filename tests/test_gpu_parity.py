@@ -299,25 +299,28 @@ def test_rescue_pass_recomputes_overflowing_rows(dsp):
     ctx.close()
 
 
-def test_pe_tie_ranks_exact_on_zero_queries(dsp):
+@pytest.mark.parametrize("n,row,keys", [(4096, 30, 13), (65536, 486, 195)])
+def test_pe_tie_ranks_exact_on_zero_queries(dsp, n, row, keys):
     """Queries of zeros make every pooled score 0, so row I of the PE triangle holds I + 1
     equal values v = 1/((I+1) N_b): each row carries 1/N_b of the mass and ties decide the
-    cut.  With N_b = 32 and gamma = 0.95, rows 0..29 are taken whole and the remaining
-    0.0125 comes from row 30's first ceil(0.0125 * 32 * 31) = 13 keys in flat order (tie
-    ranks across the head), plus the forced diagonals (row 30's, row 31's).  The GPU's
-    index set must equal the oracle's and this closed form exactly (no exemption)."""
-    n, hq, hkv = 4096, 2, 1
+    cut.  gamma = 0.95: rows 0..row-1 are taken whole (row = floor(0.95 N_b)) and the rest of
+    the mass, 0.95 - row/N_b, comes from the first ceil((0.95 - row/N_b) N_b (row+1)) keys of
+    row `row` in flat order (tie ranks across the head), plus the forced diagonals.
+    N_b = 32 (13 keys of row 30) runs the one-kernel cut of short sequences, N_b = 512 (195
+    keys of row 486) the multi-kernel radix select.  The GPU's index set must equal the
+    oracle's and this closed form exactly (no exemption)."""
+    hq, hkv = 2, 1
     nb = n // 128
+    assert row == int(0.95 * nb) and keys == int(np.ceil((0.95 - row / nb) * nb * (row + 1)))
     g = random_qkv(n, hq, hkv, 128, seed=81, scale=3.0)
     g["q"][:] = 0
     w = Workload("zero_q", n=n, hq=hq, hkv=hkv, seed=81)
-    rep, sel, osel = run_parity(dsp, w, g, flags=dsp.FLAG_FORCE_PE)
+    rep, sel, osel = run_parity(dsp, w, g, flags=dsp.FLAG_FORCE_PE,
+                                sample=None if nb <= 64 else (2, 8), seed=3)
     expect = np.tril(np.ones((nb, nb), bool))
-    expect[30] = False
-    expect[30, :13] = True
-    expect[30, 30] = True
-    expect[31] = False
-    expect[31, 31] = True
+    expect[row:] = False
+    expect[row, :keys] = True
+    expect[np.arange(row, nb), np.arange(row, nb)] = True
     gm = gpu_masks(sel, hq, nb)
     for h in range(hq):
         assert np.array_equal(np.tril(osel[h]["mask"]), expect), h
