@@ -136,15 +136,37 @@ __global__ void __launch_bounds__(1024) csr_blk_scan_kernel(int64_t* blk, int nb
 __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restrict__ rowmask,
                                                        int64_t* row_ptr,
                                                        const int64_t* __restrict__ blk,
-                                                       int64_t rows, int nbw, int32_t* col) {
+                                                       int64_t rows, int nb, int nbw,
+                                                       int32_t* col) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
   int64_t off = row_ptr[row] + blk[row >> 10];
   __syncwarp();
   if (lane == 0) row_ptr[row] = off;
-  const uint32_t lt = (1u << lane) - 1u;
   const uint32_t* m = rowmask + row * nbw;
+  // A row whose mask holds every key block K <= I (masks have no bits above I) is written
+  // as 0..I with 16-byte stores where the offset allows: the usual row of a PE head.
+  const int I = static_cast<int>(row % nb);
+  const int nw = (I >> 5) + 1;
+  int cnt = 0;
+  for (int wd = lane; wd < nw; wd += 32) cnt += __popc(m[wd]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (cnt == I + 1) {
+    const int mis = static_cast<int>((4 - (off & 3)) & 3);  // elements before a 16-byte boundary
+    const int head = mis < I + 1 ? mis : I + 1;
+    if (lane < head) col[off + lane] = lane;
+    const int body = (I + 1 - head) >> 2;
+    int4* dst4 = reinterpret_cast<int4*>(col + off + head);
+    for (int i = lane; i < body; i += 32) {
+      const int k0 = head + 4 * i;
+      dst4[i] = make_int4(k0, k0 + 1, k0 + 2, k0 + 3);
+    }
+    for (int k = head + 4 * body + lane; k <= I; k += 32) col[off + k] = k;
+    return;
+  }
+  const uint32_t lt = (1u << lane) - 1u;
   for (int wd0 = 0; wd0 < nbw; wd0 += 32) {
     const int wd = wd0 + lane;
     const uint32_t bits = wd < nbw ? m[wd] : 0u;
@@ -179,8 +201,8 @@ cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st) {
   csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.rowmask, rows, s.nbw, w.row_ptr, w.scan_blk);
   csr_blk_scan_kernel<<<1, 1024, 0, st>>>(w.scan_blk, nblk, rows, w.row_ptr);
   csr_fill_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(w.rowmask, w.row_ptr,
-                                                                        w.scan_blk, rows, s.nbw,
-                                                                        w.col);
+                                                                        w.scan_blk, rows, s.nb,
+                                                                        s.nbw, w.col);
   return cudaGetLastError();
 }
 

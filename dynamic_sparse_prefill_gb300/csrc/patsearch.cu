@@ -795,22 +795,26 @@ cudaError_t launch_patsearch(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg
   a.group = s.group;
   a.w_sink = cfg.w_sink;
   a.w_local = cfg.w_local;
-  // About three waves of CTAs (one per SM) over (head, tile chunk): among the chunk
-  // counts near that, take the one whose last wave is fullest.
-  const int want = max(1, (3 * ctx->num_sms + s.H - 1) / s.H);
-  int chunks = min(s.nb, want);
-  double best = -1.0;
-  for (int c = max(1, want / 2); c <= min(s.nb, 2 * want); ++c) {
+  // CTAs (one per SM at a time) over (head, chunk of key tiles): the chunk length that
+  // minimises waves x (per-CTA setup + tiles per CTA), the setup (barriers, TMEM, the Q
+  // tile, the pipeline's fill and drain) costing about kProxySetupTiles tiles.  Long
+  // sequences get ~4 waves of long chunks (the tail balanced); short ones one wave of fewer,
+  // longer CTAs rather than many CTAs of a few tiles that are mostly setup.
+  constexpr int kProxySetupTiles = 6;
+  int64_t best_cost = -1;
+  int tpc_best = s.nb;
+  for (int c = 1; c <= s.nb; ++c) {
     const int tpc = (s.nb + c - 1) / c;
+    if (c > 1 && tpc == (s.nb + c - 2) / (c - 1)) continue;  // same chunk length as c - 1
     const int64_t ctas = static_cast<int64_t>(s.H) * ((s.nb + tpc - 1) / tpc);
     const int64_t waves = (ctas + ctx->num_sms - 1) / ctx->num_sms;
-    const double fill = static_cast<double>(ctas) / static_cast<double>(waves * ctx->num_sms);
-    if (fill > best + 1e-9) {
-      best = fill;
-      chunks = c;
+    const int64_t cost = waves * (kProxySetupTiles + tpc);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      tpc_best = tpc;
     }
   }
-  a.tiles_per_cta = (s.nb + chunks - 1) / chunks;
+  a.tiles_per_cta = tpc_best;
   const int nchunks = (s.nb + a.tiles_per_cta - 1) / a.tiles_per_cta;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
   a.st_m = w.st_m;
