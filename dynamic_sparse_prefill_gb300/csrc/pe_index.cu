@@ -401,10 +401,11 @@ __global__ void pe_radix_init_kernel(PeState* pe, unsigned long long* hist_cnt,
   hist_mass[h * 256 + threadIdx.x] = 0.0;
 }
 
-// Rows of the PE triangle per histogram CTA (each CTA walks its rows one after the other,
-// then merges its per-warp histograms): 8 at N_b >= 1024 (at 512k, 4-8 rows per CTA took
-// 1.97-1.98 ms per selection against 2.04 with 16 and 2.23 with 1), fewer for short rows.
-int hist_rows_per_cta(int nb) { return nb >= 1024 ? 8 : (nb >= 256 ? 4 : 1); }
+// Rows of the PE triangle per histogram CTA: one per warp (each warp on its own row into
+// its own histogram copy, then the CTA merges the copies).  At 512k this took 1.83 ms per
+// selection against 1.88 with the CTA walking 8 rows together, and 1.86 with 16 rows per
+// CTA (two per warp).
+int hist_rows_per_cta(int) { return 8; }
 
 __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ pev,
                                                       const uint8_t* __restrict__ route,
@@ -457,28 +458,33 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
       m0 = v;
     }
   };
+  // A warp per row (its own histogram copy, so no cross-warp contention): four coalesced
+  // float4 loads in flight per lane, the warps of a CTA on neighbouring rows.
+  const int lane = threadIdx.x & 31;
   const int I0 = blockIdx.x * rows_per_cta;
-  for (int I = I0; I < min(nb, I0 + rows_per_cta); ++I) {
+  for (int I = I0 + wp; I < min(nb, I0 + rows_per_cta); I += 8) {
     const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
     const int len = I + 1;
     if ((nb & 3) == 0) {
-      // rows start on 16-byte boundaries: two float4 loads in flight per thread
+      // rows start on 16-byte boundaries
       const float4* row4 = reinterpret_cast<const float4*>(row);
       const int n4 = len >> 2;
-      int q = threadIdx.x;
-      for (; q + 256 < n4; q += 512) {
-        const float4 x = row4[q], y = row4[q + 256];
+      int q = lane;
+      for (; q + 96 < n4; q += 128) {
+        const float4 x = row4[q], y = row4[q + 32], z = row4[q + 64], u = row4[q + 96];
         take(x.x); take(x.y); take(x.z); take(x.w);
         take(y.x); take(y.y); take(y.z); take(y.w);
+        take(z.x); take(z.y); take(z.z); take(z.w);
+        take(u.x); take(u.y); take(u.z); take(u.w);
       }
-      if (q < n4) {
+      for (; q < n4; q += 32) {
         const float4 x = row4[q];
         take(x.x); take(x.y); take(x.z); take(x.w);
       }
-      const int K = (n4 << 2) + threadIdx.x;
+      const int K = (n4 << 2) + lane;
       if (K < len) take(row[K]);
     } else {
-      for (int K = threadIdx.x; K < len; K += 256) take(row[K]);
+      for (int K = lane; K < len; K += 32) take(row[K]);
     }
   }
   if (c0) {
@@ -662,6 +668,8 @@ __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restri
 // Row masks of PE heads: v > T, or v == T with flat rank < need; plus the diagonal.  A warp
 // per row, four 32-key words in flight per lane.  Flat-order tie ranks are needed only
 // when some but not all items equal to the threshold are taken (need_eq < count_eq).
+constexpr int kMaskWords = 4;
+
 __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ pev,
                                                       const uint8_t* __restrict__ route,
                                                       const PeState* __restrict__ pe,
@@ -684,15 +692,15 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
   // near-threshold pairs: |v - T| <= 1e-3 T (none counted when the whole triangle is kept)
   const float T = __uint_as_float(st.thresh);
   int near_cnt = 0;
-  for (int wd0 = 0; wd0 < nw; wd0 += 4) {
-    uint32_t x[4];
+  for (int wd0 = 0; wd0 < nw; wd0 += kMaskWords) {
+    uint32_t x[kMaskWords];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kMaskWords; ++u) {
       const int K = (wd0 + u) * 32 + lane;
       x[u] = K <= I ? __float_as_uint(row[K]) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kMaskWords; ++u) {
       const int wd = wd0 + u;
       if (wd >= nw) break;
       const bool valid = wd * 32 + lane <= I;
