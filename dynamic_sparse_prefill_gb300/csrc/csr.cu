@@ -18,7 +18,9 @@ constexpr int kRowsPerCta = 32;
 // Row masks of a VS head, one 32-key word per thread.  The route kernel wrote the vertical
 // selection and the slash selection reversed (bit x = sels[N_b-1-x]) as bit arrays; for
 // query block I, key K <= I is a slash key iff sels[I-K], i.e. bit N_b-1-I+K of the
-// reversed array, so a row word is a 64-bit funnel shift of that array.
+// reversed array, so a row word is a 64-bit funnel shift of that array.  Every row-mask
+// writer sets no bit above the diagonal and every reader stops at the diagonal's word
+// ((I >> 5) + 1 words for query block I), so the words past it are left unwritten.
 __global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restrict__ route,
                                                          const uint32_t* __restrict__ selbits,
                                                          int nb, int nbw, uint32_t* rowmask) {
@@ -35,15 +37,13 @@ __global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restri
   for (int idx = threadIdx.x; idx < nrows * nbw; idx += blockDim.x) {
     const int I = I0 + idx / nbw, wd = idx % nbw;
     const int K0 = wd * 32;
-    uint32_t out = 0;
-    if (K0 <= I) {
-      const int sh = nb - 1 - I + K0;  // bit of the reversed array for K = K0 (<= nb - 1)
-      out = sv[wd] | __funnelshift_r(sr[sh >> 5], sr[(sh >> 5) + 1], sh & 31);
-      if (wd == 0) out |= 1u;  // the sink block
-      const int top = I - K0;  // bits 0..top are keys K <= I
-      if (top < 31) out &= (2u << top) - 1u;
-      if (top < 32) out |= 1u << top;  // the diagonal block
-    }
+    if (K0 > I) continue;  // words past the diagonal's are neither written nor read
+    const int sh = nb - 1 - I + K0;  // bit of the reversed array for K = K0 (<= nb - 1)
+    uint32_t out = sv[wd] | __funnelshift_r(sr[sh >> 5], sr[(sh >> 5) + 1], sh & 31);
+    if (wd == 0) out |= 1u;  // the sink block
+    const int top = I - K0;  // bits 0..top are keys K <= I
+    if (top < 31) out &= (2u << top) - 1u;
+    if (top < 32) out |= 1u << top;  // the diagonal block
     rowmask[(static_cast<size_t>(h) * nb + I) * nbw + wd] = out;
   }
 }
@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restri
 // at most 16 words) and scans them inside the CTA: row_ptr[row] = offset within the CTA's
 // rows, blk[b] = the CTA's total.
 __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __restrict__ rowmask,
-                                                              int64_t rows, int nbw,
+                                                              int64_t rows, int nb, int nbw,
                                                               int64_t* row_ptr, int64_t* blk) {
   __shared__ int cnt[1024];
   __shared__ int wsum[32];
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __
     int c = 0;
     if (row < rows) {
       const uint32_t* m = rowmask + row * nbw;
-      for (int wd = 0; wd < nbw; ++wd) c += __popc(m[wd]);
+      const int nw = static_cast<int>(row) % nb / 32 + 1;
+      for (int wd = 0; wd < nw; ++wd) c += __popc(m[wd]);
     }
     cnt[threadIdx.x] = c;
   } else {
@@ -72,7 +73,8 @@ __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __
       int c = 0;
       if (row < rows) {
         const uint32_t* m = rowmask + row * nbw;
-        for (int wd = lane; wd < nbw; wd += 32) c += __popc(m[wd]);
+        const int nw = static_cast<int>(row) % nb / 32 + 1;
+        for (int wd = lane; wd < nw; wd += 32) c += __popc(m[wd]);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
   const uint32_t* m = rowmask + row * nbw;
   // A row whose mask holds every key block K <= I (masks have no bits above I) is written
   // as 0..I with 16-byte stores where the offset allows: the usual row of a PE head.
-  const int I = static_cast<int>(row % nb);
+  const int I = static_cast<int>(row) % nb;
   const int nw = (I >> 5) + 1;
   int cnt = 0;
   for (int wd = lane; wd < nw; wd += 32) cnt += __popc(m[wd]);
@@ -167,9 +169,9 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
     return;
   }
   const uint32_t lt = (1u << lane) - 1u;
-  for (int wd0 = 0; wd0 < nbw; wd0 += 32) {
+  for (int wd0 = 0; wd0 < nw; wd0 += 32) {
     const int wd = wd0 + lane;
-    const uint32_t bits = wd < nbw ? m[wd] : 0u;
+    const uint32_t bits = wd < nw ? m[wd] : 0u;
     int pre = __popc(bits);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -198,7 +200,8 @@ cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st) {
                                                                  w.rowmask);
   const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
   const int nblk = static_cast<int>((rows + 1023) / 1024);
-  csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.rowmask, rows, s.nbw, w.row_ptr, w.scan_blk);
+  csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.rowmask, rows, s.nb, s.nbw, w.row_ptr,
+                                                w.scan_blk);
   csr_blk_scan_kernel<<<1, 1024, 0, st>>>(w.scan_blk, nblk, rows, w.row_ptr);
   csr_fill_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(w.rowmask, w.row_ptr,
                                                                         w.scan_blk, rows, s.nb,
