@@ -244,8 +244,12 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
         sums(m_run, u, w);
       }
       // Anchor mass: the first w_sink keys (tile 0) and the last w_local keys (last tile).
+      // With windows of one whole tile that is the tile's own u + w (w = 0 on the causal
+      // last tile; with N_b = 1 the one tile is both and its keys count once).
       float an = 0.f;
-      if (t == 0 || last) {
+      if ((t == 0 || last) && a.w_sink == kBlk && a.w_local == kBlk) {
+        an = u + w;
+      } else if (t == 0 || last) {
         const float neg = -m_run;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
@@ -443,7 +447,9 @@ __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
 }
 
 // Blocks with p > thr, then (if fewer than kmin) the largest remaining ones until
-// k = clip(count, kmin, nb) are kept.  Returns count and k.
+// k = clip(count, kmin, nb) are kept.  Returns count and k.  Up to kWarpPadNb blocks one
+// warp adds the padding; above it the whole block takes one argmax per added block.
+constexpr int kWarpPadNb = 256;
 __device__ void select_direction(const float* p, uint8_t* sel, int nb, float thr, int kmin,
                                  int* red, float* redf, int* out_c, int* out_k) {
   int local = 0;
@@ -454,6 +460,47 @@ __device__ void select_direction(const float* p, uint8_t* sel, int nb, float thr
   }
   const int c = block_count_1024(local, red);
   const int k = min(max(c, kmin), nb);
+  if (k > c && nb <= kWarpPadNb) {
+    // The same blocks, picked by one warp without block barriers: lane l holds blocks
+    // l, l + 32, ... (at most 8), and each step takes the argmax (score descending, index
+    // ascending) of the unselected ones by shuffles.
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      float pv[8];
+      uint32_t avail = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int J = lane + 32 * j;
+        pv[j] = -1.f;
+        if (J < nb && !sel[J]) {
+          pv[j] = p[J];
+          avail |= 1u << j;
+        }
+      }
+      for (int it = c; it < k; ++it) {
+        float bv = -1.f;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (avail & (1u << j)) better(bv, bi, pv[j], lane + 32 * j);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+          better(bv, bi, v2, i2);
+        }
+        if (bi < 0 || bi >= nb) break;  // every lane holds the same winner
+        if ((bi & 31) == lane) {
+          avail &= ~(1u << (bi >> 5));
+          sel[bi] = 1;
+        }
+      }
+    }
+    __syncthreads();
+    *out_c = c;
+    *out_k = k;
+    return;
+  }
   for (int it = c; it < k; ++it) {
     float bv = -1.f;
     int bi = 0x7fffffff;
@@ -584,10 +631,26 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
   __shared__ float redf[32];
   __shared__ double part[1024];
   __shared__ int first;
-  __shared__ float sRowM[kBlk], sRowZ[kBlk];
+  __shared__ float sRowM[kBlk], sRowZ[kBlk], sRowIZ[kBlk];
   const int h = blockIdx.x;
   const int nb = a.nb;
   const size_t hb = static_cast<size_t>(h) * nb;
+  // C_struct's operands (written by the tile kernel) load first: they do not depend on the
+  // row merge below, so their latency overlaps it.
+  float anc0 = 0.f, anc1 = 0.f, stm0 = 0.f, stm1 = 0.f, rowm = 0.f, rowz = 1.f;
+  if (threadIdx.x < kBlk) {
+    const int r = threadIdx.x;
+    anc0 = a.anc[(static_cast<size_t>(h) * 2) * kBlk + r];
+    stm0 = a.st_m[hb * kBlk + r];
+    if (nb > 1) {
+      anc1 = a.anc[(static_cast<size_t>(h) * 2 + 1) * kBlk + r];
+      stm1 = a.st_m[(hb + nb - 1) * kBlk + r];
+    }
+    if (!a.fuse_rows) {
+      rowm = a.rowM[h * kBlk + r];
+      rowz = a.rowZ[h * kBlk + r];
+    }
+  }
 
   if (a.fuse_rows) {
     // Row maximum and normaliser of every proxy row over all tiles (8 slices of tiles
@@ -595,16 +658,30 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
     float* pM = reinterpret_cast<float*>(part);  // [8][128] (part's bytes, unused yet)
     float* pZ = pM + 8 * kBlk;
     const int r = threadIdx.x & (kBlk - 1), slice = threadIdx.x >> 7;
+    // Eight tiles' loads are issued before their merge steps; a missing tile is
+    // (-FLT_MAX, 0), which adds exactly 0 to Z.
     float M = -FLT_MAX, Z = 0.f;
-    for (int t = slice; t < nb; t += 8) {
-      const size_t idx = (hb + t) * kBlk + r;
-      const float m = a.st_m[idx];
-      const float sum = a.st_u[idx] + a.st_w[idx];
-      if (m > M) {
-        Z = Z * fast_exp2(M - m) + sum;
-        M = m;
-      } else {
-        Z += sum * fast_exp2(m - M);
+    for (int t0 = slice; t0 < nb; t0 += 64) {
+      float mm[8], ss[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = t0 + 8 * j;
+        mm[j] = -FLT_MAX;
+        ss[j] = 0.f;
+        if (t < nb) {
+          const size_t idx = (hb + t) * kBlk + r;
+          mm[j] = a.st_m[idx];
+          ss[j] = a.st_u[idx] + a.st_w[idx];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (mm[j] > M) {
+          Z = Z * fast_exp2(M - mm[j]) + ss[j];
+          M = mm[j];
+        } else {
+          Z += ss[j] * fast_exp2(mm[j] - M);
+        }
       }
     }
     pM[slice * kBlk + r] = M;
@@ -617,46 +694,74 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
       for (int i = 0; i < 8; ++i) Zt += pZ[i * kBlk + r] * fast_exp2(pM[i * kBlk + r] - Mt);
       sRowM[r] = Mt;
       sRowZ[r] = Zt;
+      sRowIZ[r] = 1.f / Zt;
     }
     __syncthreads();
-    float* shi = spv;  // p_v in spv; the slash halves of each tile in sps and keys' bytes
+    // p_v of every tile into spv (and global), the slash halves of each tile into the sort
+    // keys' bytes (2 * n2 >= 2 * N_b floats, unused until a flag's sort).  A warp takes two
+    // tiles per step, all their loads first.
     float* slo = reinterpret_cast<float*>(keys);
+    float* shi = slo + nb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = warp; t < nb; t += 32) {
-      float su = 0.f, sw = 0.f;
+    for (int t = warp; t < nb; t += 64) {
+      float xm[2][4], xu[2][4], xw[2][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int rr = lane + 32 * k;
-        const size_t idx = (hb + t) * kBlk + rr;
-        const float e = fast_exp2(a.st_m[idx] - sRowM[rr]) / sRowZ[rr];
-        su += a.st_u[idx] * e;
-        sw += a.st_w[idx] * e;
+      for (int j = 0; j < 2; ++j) {
+        const int tt = t + 32 * j;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xm[j][k] = 0.f;
+          xu[j][k] = 0.f;
+          xw[j][k] = 0.f;
+          if (tt < nb) {
+            const size_t idx = (hb + tt) * kBlk + lane + 32 * k;
+            xm[j][k] = a.st_m[idx];
+            xu[j][k] = a.st_u[idx];
+            xw[j][k] = a.st_w[idx];
+          }
+        }
+      }
+      float su[2] = {0.f, 0.f}, sw[2] = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = lane + 32 * k;
+          const float e = fast_exp2(xm[j][k] - sRowM[rr]) * sRowIZ[rr];  // as proxy_pool
+          su[j] += xu[j][k] * e;
+          sw[j] += xw[j][k] * e;
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        su += __shfl_xor_sync(0xffffffffu, su, o);
-        sw += __shfl_xor_sync(0xffffffffu, sw, o);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          su[j] += __shfl_xor_sync(0xffffffffu, su[j], o);
+          sw[j] += __shfl_xor_sync(0xffffffffu, sw[j], o);
+        }
       }
       if (lane == 0) {
-        a.pv[hb + t] = (su + sw) * a.inv_b;
-        sps[t] = su * a.inv_b;
-        slo[t] = sw * a.inv_b;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int tt = t + 32 * j;
+          if (tt < nb) {
+            const float pv = (su[j] + sw[j]) * a.inv_b;
+            a.pv[hb + tt] = pv;
+            spv[tt] = pv;
+            shi[tt] = su[j] * a.inv_b;
+            slo[tt] = sw[j] * a.inv_b;
+          }
+        }
       }
     }
     __syncthreads();
-    // p_v[J] = tile J's vertical mass; p_s[J] = hi part of tile N_b-1-J + lo part of N_b-2-J
+    // p_s[J] = hi part of tile N_b-1-J + lo part of N_b-2-J
     for (int J = threadIdx.x; J < nb; J += blockDim.x) {
-      float s = sps[nb - 1 - J];
+      float s = shi[nb - 1 - J];
       if (J <= nb - 2) s += slo[nb - 2 - J];
-      shi[J] = s;  // parked in spv until sps is free
+      sps[J] = s;
+      a.ps[hb + J] = s;
     }
-    __syncthreads();
-    for (int J = threadIdx.x; J < nb; J += blockDim.x) {
-      sps[J] = shi[J];
-      a.ps[hb + J] = shi[J];
-    }
-    __syncthreads();
-    for (int J = threadIdx.x; J < nb; J += blockDim.x) spv[J] = a.pv[hb + J];
     __syncthreads();
   }
 
@@ -664,13 +769,10 @@ __global__ void __launch_bounds__(1024) route_vs_select_kernel(const RouteArgs a
   float c = 0.f;
   if (threadIdx.x < kBlk) {
     const int r = threadIdx.x;
-    const float M = a.fuse_rows ? sRowM[r] : a.rowM[h * kBlk + r];
-    const float iz = 1.f / (a.fuse_rows ? sRowZ[r] : a.rowZ[h * kBlk + r]);
-    c = a.anc[(static_cast<size_t>(h) * 2) * kBlk + r] *
-        fast_exp2(a.st_m[hb * kBlk + r] - M);
-    if (nb > 1)
-      c += a.anc[(static_cast<size_t>(h) * 2 + 1) * kBlk + r] *
-           fast_exp2(a.st_m[(hb + nb - 1) * kBlk + r] - M);
+    const float M = a.fuse_rows ? sRowM[r] : rowm;
+    const float iz = 1.f / (a.fuse_rows ? sRowZ[r] : rowz);
+    c = anc0 * fast_exp2(stm0 - M);
+    if (nb > 1) c += anc1 * fast_exp2(stm1 - M);
     c *= iz;
   }
   const float C = block_sum_1024(c, redf) * a.inv_b;
