@@ -299,7 +299,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.kbar), sizeof(float) * Hkv * nb * kD},
       {reinterpret_cast<void**>(&w.pev), sizeof(float) * H * nb * nb},
       {reinterpret_cast<void**>(&w.hist_cnt), sizeof(unsigned long long) * H * 256},
-      {reinterpret_cast<void**>(&w.hist_mass), sizeof(double) * H * 256},
+      {reinterpret_cast<void**>(&w.hist_mass), sizeof(unsigned long long) * H * 256},
       {reinterpret_cast<void**>(&w.pe), sizeof(PeState) * H},
       {reinterpret_cast<void**>(&w.eq_off), sizeof(int64_t) * H * (nb + 1)},
       {reinterpret_cast<void**>(&w.rowmask), sizeof(uint32_t) * H * nb * nbw},

@@ -16,11 +16,19 @@ constexpr int kD = 128;        // head dimension
 constexpr int kBlk = 128;      // block size B = proxy rows b
 constexpr int kTileBytes = kBlk * kD * 2;  // one 128 x 128 bf16 tile
 
+// Masses of the PE gamma cut (bin masses, running sums, the target) are fixed point in
+// units of 2^-56: the probabilities v are >= 0 and a head's triangle sums to 1 (each row of
+// the pooled softmax sums to 1, scaled by 1/N_b), so every sum fits in 64 bits and adds
+// exactly, and the digit picks run on integer adds instead of fp64 (slow on this GPU).
+// An fp32 partial sum of v is rounded once, to 2^-56, when it enters the histogram.
+constexpr float kMassScale = 0x1p56f;
+constexpr unsigned long long kMassOne = 1ull << 56;
+
 // Radix-select state of one PE head's gamma cut (device).
 struct PeState {
   uint32_t prefix;          // decided high bits of the threshold
   uint32_t decided;         // mask of decided bits
-  double mass_above;        // mass of items strictly above the decided range
+  unsigned long long above;  // mass of items strictly above the decided range (fixed point)
   uint32_t thresh;          // threshold bit pattern (after the last pass)
   uint32_t select_all;      // 1: the whole triangle is taken
   unsigned long long need_eq;   // items equal to thresh to take, in flat order
@@ -62,7 +70,7 @@ struct Workspace {
   float* kbar = nullptr;     // [Hkv][nb][128] fp32 (JSD routing)
   float* pev = nullptr;      // [H][nb][nb] v = A_bar / N_b (lower triangle)
   unsigned long long* hist_cnt = nullptr;  // [H][256]
-  double* hist_mass = nullptr;             // [H][256]
+  unsigned long long* hist_mass = nullptr; // [H][256], fixed point (kMassOne = 1)
   PeState* pe = nullptr;                   // [H]
   int64_t* eq_off = nullptr;               // [H][nb+1]
   // per-row block masks and CSR

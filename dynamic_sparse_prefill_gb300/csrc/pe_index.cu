@@ -9,7 +9,7 @@
 // The pooled softmax runs on the tensor cores (pe_prob_kernel: the block means as bf16
 // hi/lo pairs, three MMA chains per tile, fp32 accumulate in TMEM) and writes v directly.
 // The sort is a radix select on the fp32 bit patterns of the (positive) flattened scores
-// with fp64 mass per digit: four 8-bit passes find the threshold value T with
+// with fixed-point mass per digit: four 8-bit passes find the threshold value T with
 // mass(v > T) < gamma <= mass(v >= T); items equal to T are then taken in flat-index
 // order (I*N_b + K) until the running mass reaches gamma.  Every PE row also gets its
 // diagonal pair, so that no query block is left without keys.
@@ -391,14 +391,14 @@ __global__ void __launch_bounds__(kPeThreads, 1)
 
 // ---------------------------------------------------------------- radix select
 __global__ void pe_radix_init_kernel(PeState* pe, unsigned long long* hist_cnt,
-                                     double* hist_mass) {
+                                     unsigned long long* hist_mass) {
   const int h = blockIdx.x;
   if (threadIdx.x == 0) {
     PeState s{};
     pe[h] = s;
   }
   hist_cnt[h * 256 + threadIdx.x] = 0;
-  hist_mass[h * 256 + threadIdx.x] = 0.0;
+  hist_mass[h * 256 + threadIdx.x] = 0ull;
 }
 
 // Rows of the PE triangle per histogram CTA: one per warp (each warp on its own row into
@@ -412,15 +412,14 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
                                                       const PeState* __restrict__ pe, int nb,
                                                       int rows_per_cta, int shift,
                                                       unsigned long long* hist_cnt,
-                                                      double* hist_mass) {
+                                                      unsigned long long* hist_mass) {
   const int h = blockIdx.y;
   if (route[h]) return;
   const PeState st = pe[h];
   if (st.select_all) return;
   // Per-warp histograms with native fp32 shared-memory atomics (later passes see many
   // values in few bins, so one shared copy serialises the warps); the CTA's partial
-  // masses (each at most a few percent of the total) are combined in fp64 in global
-  // memory.
+  // masses (each at most a few percent of the total) go to global memory in fixed point.
   __shared__ unsigned int scnt[8][256];
   __shared__ float smass[8][256];
   const int wp = threadIdx.x >> 5;
@@ -497,53 +496,60 @@ __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ 
   }
   __syncthreads();
   unsigned int c = 0;
-  double m = 0.0;
+  float m = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     c += scnt[w][threadIdx.x];
-    m += static_cast<double>(smass[w][threadIdx.x]);
+    m += smass[w][threadIdx.x];
   }
   if (c) {
     atomicAdd(&hist_cnt[h * 256 + threadIdx.x], static_cast<unsigned long long>(c));
-    atomicAdd(&hist_mass[h * 256 + threadIdx.x], m);
+    atomicAdd(&hist_mass[h * 256 + threadIdx.x], __float2ull_rn(m * kMassScale));
   }
 }
 
+// gamma in mass units (exact for an fp32 gamma in (0, 1] down to 2^-32; rounded up below).
+__device__ __forceinline__ unsigned long long gamma_fixed(float gamma) {
+  return __float2ull_ru(gamma * kMassScale);
+}
+
 // Picks the digit whose bin crosses the remaining target.  One warp per head: lane l holds
-// bins 255-8l .. 248-8l (descending), the lanes' fp64 masses are prefix-summed by shuffles,
-// and the first lane whose bins cross the target supplies the digit (the walk from the top
-// bin down that the cumulative-coverage rule describes, with the sums grouped by lane).
+// bins 255-8l .. 248-8l (descending), the lanes' fixed-point masses are prefix-summed by
+// shuffles, and the first lane whose bins cross the target supplies the digit (the walk
+// from the top bin down that the cumulative-coverage rule describes, with the sums grouped
+// by lane).
 __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, float gamma,
-                                PeState* pe, unsigned long long* hist_cnt, double* hist_mass) {
+                                PeState* pe, unsigned long long* hist_cnt,
+                                unsigned long long* hist_mass) {
   const int h = blockIdx.x;
   if (route[h] == 0 && threadIdx.x < 32) {
     const int lane = threadIdx.x;
     PeState st = pe[h];
     if (!st.select_all) {
       const int shift = 24 - 8 * pass;
-      const double rem = static_cast<double>(gamma) - st.mass_above;
+      const unsigned long long rem = gamma_fixed(gamma) - st.above;
       unsigned long long c[8];
-      double m[8];
+      unsigned long long m[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int bin = 255 - (lane * 8 + i);
         c[i] = hist_cnt[h * 256 + bin];
         m[i] = hist_mass[h * 256 + bin];
       }
-      double local = 0.0;
+      unsigned long long local = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (c[i]) local += m[i];
-      double incl = local;
+      unsigned long long incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      double cum = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) cum = 0.0;
+      unsigned long long cum = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) cum = 0;
       int cand = -1, low = -1;
-      double cand_cum = 0.0, low_m = 0.0;
+      unsigned long long cand_cum = 0, low_m = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (!c[i]) continue;
@@ -560,7 +566,7 @@ __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, flo
         low_m = m[i];
       }
       int chosen = -1;
-      double above = 0.0;
+      unsigned long long above = 0;
       const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
       if (hit) {
         const int src = __ffs(hit) - 1;
@@ -568,7 +574,7 @@ __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, flo
         above = __shfl_sync(0xffffffffu, cand_cum, src);
       } else {
         const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
-        const double total = __shfl_sync(0xffffffffu, incl, 31);
+        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
         if (pass == 0 || any == 0) {
           st.select_all = 1;  // the whole triangle holds less than gamma
         } else {
@@ -579,14 +585,14 @@ __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, flo
       }
       if (lane == 0) {
         if (!st.select_all) {
-          st.mass_above += above;
+          st.above += above;
           st.prefix |= static_cast<uint32_t>(chosen) << shift;
           st.decided |= 255u << shift;
           if (pass == 3) {
             st.thresh = st.prefix;
             st.count_eq = hist_cnt[h * 256 + chosen];
             const double vt = static_cast<double>(__uint_as_float(st.thresh));
-            const double rem2 = static_cast<double>(gamma) - st.mass_above;
+            const double rem2 = static_cast<double>(gamma_fixed(gamma) - st.above) * 0x1p-56;
             unsigned long long need = st.count_eq;
             if (vt > 0.0) {
               const double q = ceil(rem2 / vt);
@@ -601,7 +607,7 @@ __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, flo
   }
   __syncthreads();
   hist_cnt[h * 256 + threadIdx.x] = 0;
-  hist_mass[h * 256 + threadIdx.x] = 0.0;
+  hist_mass[h * 256 + threadIdx.x] = 0ull;
 }
 
 // Number of items equal to the threshold in each PE row (for flat-order tie ranks): a warp
@@ -723,7 +729,6 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
       if (lane == 0) mrow[wd] = word;
     }
   }
-  for (int wd = nw + lane; wd < nbw; wd += 32) mrow[wd] = 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) near_cnt += __shfl_xor_sync(0xffffffffu, near_cnt, o);
   if (lane == 0) {
@@ -737,11 +742,11 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
 // N_b <= kSmallNb: the whole gamma cut of a PE head in one CTA, the triangle held in shared
 // memory (flattened row by row: pair (I, K) at I (I + 1) / 2 + K, the flat order of the
 // cut's ties).  Same steps and rules as the multi-kernel path above: four 8-bit radix
-// passes with fp64 bin masses and the same digit pick, flat-order tie ranks when only some
-// of the items equal to the threshold are taken, then the row masks (plus the diagonal),
-// the kept-pair and rescued-row counts and the near-threshold count.  One launch instead
-// of twelve, which matters at short lengths, where each launch costs about as much as its
-// work.
+// passes with fixed-point bin masses and the same digit pick, flat-order tie ranks when
+// only some of the items equal to the threshold are taken, then the row masks (plus the
+// diagonal), the kept-pair and rescued-row counts and the near-threshold count.  One
+// launch instead of twelve, which matters at short lengths, where each launch costs about
+// as much as its work.
 constexpr int kSmallNb = 256;
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallCopies = 8;  // shared histogram copies (one per 4 warps)
@@ -821,7 +826,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
     }
     __syncthreads();
-    // the copies combined per bin (count, fp32 mass) before the fp64 pick
+    // the copies combined per bin (count, fp32 mass) before the fixed-point pick
     if (tid < 256) {
       uint32_t cc = 0;
       float mm = 0.f;
@@ -837,29 +842,29 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     if (warp == 0) {
       // the digit whose bin crosses the remaining target, bins walked from the top: lane l
       // holds bins 255 - 8l .. 248 - 8l (the same pick as pe_digit_kernel)
-      const double rem = static_cast<double>(gamma) - st.mass_above;
+      const unsigned long long rem = gamma_fixed(gamma) - st.above;
       unsigned long long c[8];
-      double m[8];
+      unsigned long long m[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int bin = 255 - (lane * 8 + i);
         c[i] = scnt[0][bin];
-        m[i] = static_cast<double>(smass[0][bin]);
+        m[i] = __float2ull_rn(smass[0][bin] * kMassScale);
       }
-      double local = 0.0;
+      unsigned long long local = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (c[i]) local += m[i];
-      double incl = local;
+      unsigned long long incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      double cum = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) cum = 0.0;
+      unsigned long long cum = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) cum = 0;
       int cand = -1, low = -1;
-      double cand_cum = 0.0, low_m = 0.0;
+      unsigned long long cand_cum = 0, low_m = 0;
       unsigned long long cand_c = 0, low_c = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -879,7 +884,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         low_c = c[i];
       }
       int chosen = -1;
-      double above = 0.0;
+      unsigned long long above = 0;
       unsigned long long chosen_c = 0;
       bool all = false;
       const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
@@ -890,7 +895,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         chosen_c = __shfl_sync(0xffffffffu, cand_c, src);
       } else {
         const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
-        const double total = __shfl_sync(0xffffffffu, incl, 31);
+        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
         if (pass == 0 || any == 0) {
           all = true;  // the whole triangle holds less than gamma
         } else {
@@ -905,14 +910,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         if (all) {
           ns.select_all = 1;
         } else {
-          ns.mass_above += above;
+          ns.above += above;
           ns.prefix |= static_cast<uint32_t>(chosen) << shift;
           ns.decided |= 255u << shift;
           if (pass == 3) {
             ns.thresh = ns.prefix;
             ns.count_eq = chosen_c;
             const double vt = static_cast<double>(__uint_as_float(ns.thresh));
-            const double rem2 = static_cast<double>(gamma) - ns.mass_above;
+            const double rem2 = static_cast<double>(gamma_fixed(gamma) - ns.above) * 0x1p-56;
             unsigned long long need = ns.count_eq;
             if (vt > 0.0) {
               const double q = ceil(rem2 / vt);
@@ -932,48 +937,60 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const bool rank_ties = !all && st.need_eq < st.count_eq;
   const float Tv = __uint_as_float(st.thresh);
 
-  // 3. kept pairs as bits in flat order; every thread owns whole 32-pair words of a
-  // contiguous range (flat-order tie ranks by a scan of the per-thread tie counts)
+  // 3. kept pairs as bits in flat order.  Without tie ranks (all items equal to the
+  // threshold are kept, or the whole triangle is) a warp builds a 32-pair word from one
+  // coalesced read (lane k: pair 32 w + k) and a ballot; with them, every thread owns whole
+  // words of a contiguous range and the ranks come from a scan of the per-thread tie counts.
   const int words = (T + 31) / 32;
-  const int wper = (words + kSmallThreads - 1) / kSmallThreads;
-  const int f0 = min(T, tid * wper * 32), f1 = min(T, (tid + 1) * wper * 32);
-  int eq = 0;
-  if (rank_ties)
+  int near_cnt = 0;
+  if (!rank_ties) {
+    for (int wd = warp; wd < words; wd += kSmallThreads / 32) {
+      const int f = wd * 32 + lane;
+      const uint32_t bits = f < T ? sv[f] : 0u;
+      const bool sel = f < T && (all || bits >= st.thresh);
+      if (f < T && !all && fabsf(__uint_as_float(bits) - Tv) <= 1e-3f * Tv) ++near_cnt;
+      const unsigned word = __ballot_sync(0xffffffffu, sel);
+      if (lane == 0) sbits[wd] = word;
+    }
+  } else {
+    const int wper = (words + kSmallThreads - 1) / kSmallThreads;
+    const int f0 = min(T, tid * wper * 32), f1 = min(T, (tid + 1) * wper * 32);
+    int eq = 0;
     for (int f = f0; f < f1; ++f) eq += sv[f] == st.thresh ? 1 : 0;
-  // exclusive scan of eq over the threads
-  int incl = eq;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_red[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = s_red[lane];
+    // exclusive scan of eq over the threads
+    int incl = eq;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    s_red[lane] = w;
-  }
-  __syncthreads();
-  long long rank = (warp > 0 ? s_red[warp - 1] : 0) + incl - eq;
-  int near_cnt = 0;
-  for (int f = f0; f < f1; f += 32) {
-    uint32_t word = 0;
-    for (int k = 0; k < 32 && f + k < f1; ++k) {
-      const uint32_t bits = sv[f + k];
-      bool sel = all || bits > st.thresh;
-      if (!all && bits == st.thresh) {
-        sel = rank_ties ? rank < static_cast<long long>(st.need_eq) : true;
-        ++rank;
+    if (lane == 31) s_red[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_red[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
       }
-      if (!all && fabsf(__uint_as_float(bits) - Tv) <= 1e-3f * Tv) ++near_cnt;
-      if (sel) word |= 1u << k;
+      s_red[lane] = w;
     }
-    sbits[f >> 5] = word;
+    __syncthreads();
+    long long rank = (warp > 0 ? s_red[warp - 1] : 0) + incl - eq;
+    for (int f = f0; f < f1; f += 32) {
+      uint32_t word = 0;
+      for (int k = 0; k < 32 && f + k < f1; ++k) {
+        const uint32_t bits = sv[f + k];
+        bool sel = all || bits > st.thresh;
+        if (!all && bits == st.thresh) {
+          sel = rank < static_cast<long long>(st.need_eq);
+          ++rank;
+        }
+        if (!all && fabsf(__uint_as_float(bits) - Tv) <= 1e-3f * Tv) ++near_cnt;
+        if (sel) word |= 1u << k;
+      }
+      sbits[f >> 5] = word;
+    }
   }
   __syncthreads();
 
