@@ -301,6 +301,7 @@ crisp_status crisp_create(const crisp_dims* max_dims, crisp_ctx* out) {
       {reinterpret_cast<void**>(&w.hist_cnt), sizeof(unsigned long long) * H * 256},
       {reinterpret_cast<void**>(&w.hist_mass), sizeof(unsigned long long) * H * 256},
       {reinterpret_cast<void**>(&w.pe), sizeof(PeState) * H},
+      {reinterpret_cast<void**>(&w.pe_list), sizeof(int) * (H + 1)},
       {reinterpret_cast<void**>(&w.eq_off), sizeof(int64_t) * H * (nb + 1)},
       {reinterpret_cast<void**>(&w.rowmask), sizeof(uint32_t) * H * nb * nbw},
       {reinterpret_cast<void**>(&w.scan_blk), sizeof(int64_t) * ((H * nb + 1023) / 1024 + 1)},

@@ -21,8 +21,6 @@ constexpr int kTileBytes = kBlk * kD * 2;  // one 128 x 128 bf16 tile
 // the pooled softmax sums to 1, scaled by 1/N_b), so every sum fits in 64 bits and adds
 // exactly, and the digit picks run on integer adds instead of fp64 (slow on this GPU).
 // An fp32 partial sum of v is rounded once, to 2^-56, when it enters the histogram.
-constexpr float kMassScale = 0x1p56f;
-constexpr unsigned long long kMassOne = 1ull << 56;
 
 // Radix-select state of one PE head's gamma cut (device).
 struct PeState {
@@ -70,8 +68,9 @@ struct Workspace {
   float* kbar = nullptr;     // [Hkv][nb][128] fp32 (JSD routing)
   float* pev = nullptr;      // [H][nb][nb] v = A_bar / N_b (lower triangle)
   unsigned long long* hist_cnt = nullptr;  // [H][256]
-  unsigned long long* hist_mass = nullptr; // [H][256], fixed point (kMassOne = 1)
+  unsigned long long* hist_mass = nullptr; // [H][256], fixed point (2^-56 units)
   PeState* pe = nullptr;                   // [H]
+  int* pe_list = nullptr;                  // [H + 1]: count of PE heads, then the heads
   int64_t* eq_off = nullptr;               // [H][nb+1]
   // per-row block masks and CSR
   uint32_t* rowmask = nullptr;  // [H][nb][nbw]

@@ -15,6 +15,7 @@
 // diagonal pair, so that no query block is left without keys.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cfloat>
 
 #include "internal.h"
@@ -47,8 +48,10 @@ __global__ void __launch_bounds__(128) pe_pool_kernel(const uint16_t* __restrict
                                                       const uint8_t* __restrict__ route, int n,
                                                       int nb, int H, int hq, int hkv, int group,
                                                       int Hkv, float q_scale, uint16_t* qs,
-                                                      uint16_t* ks) {
+                                                      uint16_t* ks, int* pe_list) {
   const int y = blockIdx.x, I = blockIdx.y;
+  // the PE head list is rebuilt by pe_radix_init_kernel, which runs after this kernel
+  if (y == 0 && I == 0 && threadIdx.x == 0) pe_list[0] = 0;
   const bool is_q = y < H;
   const uint16_t* src;
   if (is_q) {
@@ -390,127 +393,162 @@ __global__ void __launch_bounds__(kPeThreads, 1)
 }
 
 // ---------------------------------------------------------------- radix select
-__global__ void pe_radix_init_kernel(PeState* pe, unsigned long long* hist_cnt,
-                                     unsigned long long* hist_mass) {
+__global__ void pe_radix_init_kernel(const uint8_t* __restrict__ route, PeState* pe,
+                                     unsigned long long* hist_cnt,
+                                     unsigned long long* hist_mass, int* pe_list) {
   const int h = blockIdx.x;
   if (threadIdx.x == 0) {
     PeState s{};
     pe[h] = s;
+    // the list of PE heads that the histogram, tie-count and mask kernels walk (its order
+    // does not matter: every item's arithmetic is its own, and the bin sums are integers)
+    if (!route[h]) pe_list[1 + atomicAdd(&pe_list[0], 1)] = h;
   }
   hist_cnt[h * 256 + threadIdx.x] = 0;
   hist_mass[h * 256 + threadIdx.x] = 0ull;
 }
 
-// Rows of the PE triangle per histogram CTA: one per warp (each warp on its own row into
-// its own histogram copy, then the CTA merges the copies).  At 512k this took 1.83 ms per
-// selection against 1.88 with the CTA walking 8 rows together, and 1.86 with 16 rows per
-// CTA (two per warp).
-int hist_rows_per_cta(int) { return 8; }
+// A non-negative fp32 mass in units of 2^-56 from its bits (integer arithmetic only): the
+// value is mant * 2^(e - 150), so the fixed-point number is mant shifted by e - 94; exact
+// whenever m * 2^56 is an integer (m >= 2^-33), otherwise rounded half up; 0 below 2^-126.
+// Masses here are at most ~1; anything from 2^7 up saturates at 2^63.
+__device__ __forceinline__ unsigned long long mass_fixed(float m) {
+  const uint32_t b = __float_as_uint(m) & 0x7FFFFFFFu;
+  const int e = static_cast<int>(b >> 23);
+  if (e == 0) return 0ull;
+  const unsigned long long mant = (b & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 94;
+  if (sh > 39) return 1ull << 63;
+  if (sh >= 0) return mant << sh;
+  if (sh < -24) return 0ull;
+  return (mant + (1ull << (-sh - 1))) >> (-sh);
+}
+
+// The histogram, tie-count and mask kernels walk items of 8 PE rows (a warp per row) of
+// the listed PE heads with a grid of resident CTAs (the occupancy of each kernel, found
+// once at context creation), longest rows first across all heads: a grid over every
+// (head, row chunk) launched as many CTAs that only returned for the VS heads (at 512k,
+// 12288 of 16384), at ~1.5 ns each.
+constexpr int kPeRowsPerItem = 8;
+int g_hist_ctas_per_sm = 1, g_eqcount_ctas_per_sm = 1, g_mask_ctas_per_sm = 1;
+
+__device__ __forceinline__ int pe_items(const int* pe_list, int nb) {
+  return pe_list[0] * ((nb + kPeRowsPerItem - 1) / kPeRowsPerItem);
+}
+// Item -> (head, first row): chunks in descending order, the heads interleaved.
+__device__ __forceinline__ void pe_item(const int* pe_list, int nb, int item, int& h, int& I0) {
+  const int npe = pe_list[0];
+  const int chunks = (nb + kPeRowsPerItem - 1) / kPeRowsPerItem;
+  h = pe_list[1 + item % npe];
+  I0 = (chunks - 1 - item / npe) * kPeRowsPerItem;
+}
 
 __global__ void __launch_bounds__(256) pe_hist_kernel(const float* __restrict__ pev,
-                                                      const uint8_t* __restrict__ route,
-                                                      const PeState* __restrict__ pe, int nb,
-                                                      int rows_per_cta, int shift,
-                                                      unsigned long long* hist_cnt,
+                                                      const PeState* __restrict__ pe,
+                                                      const int* __restrict__ pe_list, int nb,
+                                                      int shift, unsigned long long* hist_cnt,
                                                       unsigned long long* hist_mass) {
-  const int h = blockIdx.y;
-  if (route[h]) return;
-  const PeState st = pe[h];
-  if (st.select_all) return;
   // Per-warp histograms with native fp32 shared-memory atomics (later passes see many
   // values in few bins, so one shared copy serialises the warps); the CTA's partial
   // masses (each at most a few percent of the total) go to global memory in fixed point.
   __shared__ unsigned int scnt[8][256];
   __shared__ float smass[8][256];
-  const int wp = threadIdx.x >> 5;
+  const int wp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int items = pe_items(pe_list, nb);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    int h, I0;
+    pe_item(pe_list, nb, item, h, I0);
+    const PeState st = pe[h];
+    if (st.select_all) continue;  // the same for the whole CTA
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    scnt[w][threadIdx.x] = 0;
-    smass[w][threadIdx.x] = 0.f;
-  }
-  __syncthreads();
-  // Each thread caches two (bin, count, fp32 mass) entries and flushes one to the shared
-  // histogram only when a third bin appears: the early passes see long runs of one bin,
-  // the later ones values alternating between neighbouring bins.
-  uint32_t b0 = 0xFFFFFFFFu, b1 = 0xFFFFFFFFu, c0 = 0, c1 = 0;
-  float m0 = 0.f, m1 = 0.f;
-  auto take = [&](float v) {
-    const uint32_t bits = __float_as_uint(v);
-    if ((bits & st.decided) != st.prefix) return;
-    const uint32_t bin = (bits >> shift) & 255u;
-    if (bin == b0) {
-      ++c0;
-      m0 += v;
-    } else if (bin == b1) {
-      ++c1;
-      m1 += v;
-    } else {
-      if (c1) {
-        atomicAdd(&scnt[wp][b1], c1);
-        atomicAdd(&smass[wp][b1], m1);
-      }
-      b1 = b0;
-      c1 = c0;
-      m1 = m0;
-      b0 = bin;
-      c0 = 1;
-      m0 = v;
+    for (int w = 0; w < 8; ++w) {
+      scnt[w][threadIdx.x] = 0;
+      smass[w][threadIdx.x] = 0.f;
     }
-  };
-  // A warp per row (its own histogram copy, so no cross-warp contention): four coalesced
-  // float4 loads in flight per lane, the warps of a CTA on neighbouring rows.
-  const int lane = threadIdx.x & 31;
-  const int I0 = blockIdx.x * rows_per_cta;
-  for (int I = I0 + wp; I < min(nb, I0 + rows_per_cta); I += 8) {
-    const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
-    const int len = I + 1;
-    if ((nb & 3) == 0) {
-      // rows start on 16-byte boundaries
-      const float4* row4 = reinterpret_cast<const float4*>(row);
-      const int n4 = len >> 2;
-      int q = lane;
-      for (; q + 96 < n4; q += 128) {
-        const float4 x = row4[q], y = row4[q + 32], z = row4[q + 64], u = row4[q + 96];
-        take(x.x); take(x.y); take(x.z); take(x.w);
-        take(y.x); take(y.y); take(y.z); take(y.w);
-        take(z.x); take(z.y); take(z.z); take(z.w);
-        take(u.x); take(u.y); take(u.z); take(u.w);
+    __syncthreads();
+    // Each thread caches two (bin, count, fp32 mass) entries and flushes one to the shared
+    // histogram only when a third bin appears: the early passes see long runs of one bin,
+    // the later ones values alternating between neighbouring bins.
+    uint32_t b0 = 0xFFFFFFFFu, b1 = 0xFFFFFFFFu, c0 = 0, c1 = 0;
+    float m0 = 0.f, m1 = 0.f;
+    auto take = [&](float v) {
+      const uint32_t bits = __float_as_uint(v);
+      if ((bits & st.decided) != st.prefix) return;
+      const uint32_t bin = (bits >> shift) & 255u;
+      if (bin == b0) {
+        ++c0;
+        m0 += v;
+      } else if (bin == b1) {
+        ++c1;
+        m1 += v;
+      } else {
+        if (c1) {
+          atomicAdd(&scnt[wp][b1], c1);
+          atomicAdd(&smass[wp][b1], m1);
+        }
+        b1 = b0;
+        c1 = c0;
+        m1 = m0;
+        b0 = bin;
+        c0 = 1;
+        m0 = v;
       }
-      for (; q < n4; q += 32) {
-        const float4 x = row4[q];
-        take(x.x); take(x.y); take(x.z); take(x.w);
+    };
+    // A warp per row (its own histogram copy, so no cross-warp contention): four coalesced
+    // float4 loads in flight per lane, the warps of a CTA on neighbouring rows.
+    const int I = I0 + wp;
+    if (I < nb) {
+      const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
+      const int len = I + 1;
+      if ((nb & 3) == 0) {
+        // rows start on 16-byte boundaries
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        const int n4 = len >> 2;
+        int q = lane;
+        for (; q + 96 < n4; q += 128) {
+          const float4 x = row4[q], y = row4[q + 32], z = row4[q + 64], u = row4[q + 96];
+          take(x.x); take(x.y); take(x.z); take(x.w);
+          take(y.x); take(y.y); take(y.z); take(y.w);
+          take(z.x); take(z.y); take(z.z); take(z.w);
+          take(u.x); take(u.y); take(u.z); take(u.w);
+        }
+        for (; q < n4; q += 32) {
+          const float4 x = row4[q];
+          take(x.x); take(x.y); take(x.z); take(x.w);
+        }
+        const int K = (n4 << 2) + lane;
+        if (K < len) take(row[K]);
+      } else {
+        for (int K = lane; K < len; K += 32) take(row[K]);
       }
-      const int K = (n4 << 2) + lane;
-      if (K < len) take(row[K]);
-    } else {
-      for (int K = lane; K < len; K += 32) take(row[K]);
     }
-  }
-  if (c0) {
-    atomicAdd(&scnt[wp][b0], c0);
-    atomicAdd(&smass[wp][b0], m0);
-  }
-  if (c1) {
-    atomicAdd(&scnt[wp][b1], c1);
-    atomicAdd(&smass[wp][b1], m1);
-  }
-  __syncthreads();
-  unsigned int c = 0;
-  float m = 0.f;
+    if (c0) {
+      atomicAdd(&scnt[wp][b0], c0);
+      atomicAdd(&smass[wp][b0], m0);
+    }
+    if (c1) {
+      atomicAdd(&scnt[wp][b1], c1);
+      atomicAdd(&smass[wp][b1], m1);
+    }
+    __syncthreads();
+    unsigned int c = 0;
+    float m = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    c += scnt[w][threadIdx.x];
-    m += smass[w][threadIdx.x];
-  }
-  if (c) {
-    atomicAdd(&hist_cnt[h * 256 + threadIdx.x], static_cast<unsigned long long>(c));
-    atomicAdd(&hist_mass[h * 256 + threadIdx.x], __float2ull_rn(m * kMassScale));
+    for (int w = 0; w < 8; ++w) {
+      c += scnt[w][threadIdx.x];
+      m += smass[w][threadIdx.x];
+    }
+    if (c) {
+      atomicAdd(&hist_cnt[h * 256 + threadIdx.x], static_cast<unsigned long long>(c));
+      atomicAdd(&hist_mass[h * 256 + threadIdx.x], mass_fixed(m));
+    }
+    __syncthreads();  // the copies are read before the next item clears them
   }
 }
 
-// gamma in mass units (exact for an fp32 gamma in (0, 1] down to 2^-32; rounded up below).
+// gamma in mass units.
 __device__ __forceinline__ unsigned long long gamma_fixed(float gamma) {
-  return __float2ull_ru(gamma * kMassScale);
+  return mass_fixed(gamma);
 }
 
 // Picks the digit whose bin crosses the remaining target.  One warp per head: lane l holds
@@ -613,32 +651,35 @@ __global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, flo
 // Number of items equal to the threshold in each PE row (for flat-order tie ranks): a warp
 // per row, four coalesced loads in flight per lane.
 __global__ void __launch_bounds__(256) pe_eqcount_kernel(const float* __restrict__ pev,
-                                                         const uint8_t* __restrict__ route,
                                                          const PeState* __restrict__ pe,
+                                                         const int* __restrict__ pe_list,
                                                          int nb, int64_t* eq_off) {
-  const int h = blockIdx.y;
-  if (route[h]) return;
-  const PeState st = pe[h];
-  if (st.select_all || st.need_eq >= st.count_eq) return;  // no tie ranks needed
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int I = blockIdx.x * 8 + warp;
-  if (I >= nb) return;
-  const uint32_t* row =
-      reinterpret_cast<const uint32_t*>(pev + (static_cast<size_t>(h) * nb + I) * nb);
-  int c = 0;
-  for (int K0 = 0; K0 <= I; K0 += 128) {
-    uint32_t x[4];
+  const int items = pe_items(pe_list, nb);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    int h, I0;
+    pe_item(pe_list, nb, item, h, I0);
+    const PeState st = pe[h];
+    if (st.select_all || st.need_eq >= st.count_eq) continue;  // no tie ranks needed
+    const int I = I0 + warp;
+    if (I >= nb) continue;
+    const uint32_t* row =
+        reinterpret_cast<const uint32_t*>(pev + (static_cast<size_t>(h) * nb + I) * nb);
+    int c = 0;
+    for (int K0 = 0; K0 <= I; K0 += 128) {
+      uint32_t x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int K = K0 + u * 32 + lane;
-      x[u] = K <= I ? row[K] : ~st.thresh;
+      for (int u = 0; u < 4; ++u) {
+        const int K = K0 + u * 32 + lane;
+        x[u] = K <= I ? row[K] : ~st.thresh;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) c += x[u] == st.thresh ? 1 : 0;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) c += x[u] == st.thresh ? 1 : 0;
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) eq_off[static_cast<size_t>(h) * (nb + 1) + I] = c;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if (lane == 0) eq_off[static_cast<size_t>(h) * (nb + 1) + I] = c;
 }
 
 __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restrict__ route,
@@ -677,64 +718,67 @@ __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restri
 constexpr int kMaskWords = 4;
 
 __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ pev,
-                                                      const uint8_t* __restrict__ route,
                                                       const PeState* __restrict__ pe,
+                                                      const int* __restrict__ pe_list,
                                                       const int64_t* __restrict__ eq_off,
                                                       int nb, int nbw, uint32_t* rowmask,
                                                       int32_t* counts, int32_t* near) {
-  const int h = blockIdx.y;
-  if (route[h]) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int I = blockIdx.x * 8 + warp;
-  if (I >= nb) return;
-  const PeState st = pe[h];
-  const bool all = st.select_all != 0;
-  const bool rank_ties = !all && st.need_eq < st.count_eq;
-  int64_t eq_base = rank_ties ? eq_off[static_cast<size_t>(h) * (nb + 1) + I] : 0;
-  const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
-  uint32_t* mrow = rowmask + (static_cast<size_t>(h) * nb + I) * nbw;
-  const int nw = (I >> 5) + 1;  // words holding keys K <= I
-  int selected = 0;
-  // near-threshold pairs: |v - T| <= 1e-3 T (none counted when the whole triangle is kept)
-  const float T = __uint_as_float(st.thresh);
-  int near_cnt = 0;
-  for (int wd0 = 0; wd0 < nw; wd0 += kMaskWords) {
-    uint32_t x[kMaskWords];
+  const int items = pe_items(pe_list, nb);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    int h, I0;
+    pe_item(pe_list, nb, item, h, I0);
+    const int I = I0 + warp;
+    if (I >= nb) continue;
+    const PeState st = pe[h];
+    const bool all = st.select_all != 0;
+    const bool rank_ties = !all && st.need_eq < st.count_eq;
+    int64_t eq_base = rank_ties ? eq_off[static_cast<size_t>(h) * (nb + 1) + I] : 0;
+    const float* row = pev + (static_cast<size_t>(h) * nb + I) * nb;
+    uint32_t* mrow = rowmask + (static_cast<size_t>(h) * nb + I) * nbw;
+    const int nw = (I >> 5) + 1;  // words holding keys K <= I
+    int selected = 0;
+    // near-threshold pairs: |v - T| <= 1e-3 T (none counted when the whole triangle is kept)
+    const float T = __uint_as_float(st.thresh);
+    int near_cnt = 0;
+    for (int wd0 = 0; wd0 < nw; wd0 += kMaskWords) {
+      uint32_t x[kMaskWords];
 #pragma unroll
-    for (int u = 0; u < kMaskWords; ++u) {
-      const int K = (wd0 + u) * 32 + lane;
-      x[u] = K <= I ? __float_as_uint(row[K]) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kMaskWords; ++u) {
-      const int wd = wd0 + u;
-      if (wd >= nw) break;
-      const bool valid = wd * 32 + lane <= I;
-      bool sel = valid && (all || x[u] > st.thresh);
-      near_cnt += (valid && !all && fabsf(__uint_as_float(x[u]) - T) <= 1e-3f * T) ? 1 : 0;
-      if (!all) {
-        const bool eq = valid && x[u] == st.thresh;
-        if (rank_ties) {
-          const unsigned beq = __ballot_sync(0xffffffffu, eq);
-          const int64_t rank = eq_base + __popc(beq & ((1u << lane) - 1u));
-          sel = sel || (eq && rank < static_cast<int64_t>(st.need_eq));
-          eq_base += __popc(beq);
-        } else {
-          sel = sel || eq;
-        }
+      for (int u = 0; u < kMaskWords; ++u) {
+        const int K = (wd0 + u) * 32 + lane;
+        x[u] = K <= I ? __float_as_uint(row[K]) : 0u;
       }
-      unsigned word = __ballot_sync(0xffffffffu, sel);
-      selected += __popc(word);
-      if (wd == (I >> 5)) word |= 1u << (I & 31);
-      if (lane == 0) mrow[wd] = word;
-    }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) near_cnt += __shfl_xor_sync(0xffffffffu, near_cnt, o);
-  if (lane == 0) {
-    if (near_cnt) atomicAdd(&near[h * 3 + 2], near_cnt);
-    atomicAdd(&counts[h * 4 + 0], selected);
-    if (selected == 0) atomicAdd(&counts[h * 4 + 1], 1);
+      for (int u = 0; u < kMaskWords; ++u) {
+        const int wd = wd0 + u;
+        if (wd >= nw) break;
+        const bool valid = wd * 32 + lane <= I;
+        bool sel = valid && (all || x[u] > st.thresh);
+        near_cnt += (valid && !all && fabsf(__uint_as_float(x[u]) - T) <= 1e-3f * T) ? 1 : 0;
+        if (!all) {
+          const bool eq = valid && x[u] == st.thresh;
+          if (rank_ties) {
+            const unsigned beq = __ballot_sync(0xffffffffu, eq);
+            const int64_t rank = eq_base + __popc(beq & ((1u << lane) - 1u));
+            sel = sel || (eq && rank < static_cast<int64_t>(st.need_eq));
+            eq_base += __popc(beq);
+          } else {
+            sel = sel || eq;
+          }
+        }
+        unsigned word = __ballot_sync(0xffffffffu, sel);
+        selected += __popc(word);
+        if (wd == (I >> 5)) word |= 1u << (I & 31);
+        if (lane == 0) mrow[wd] = word;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) near_cnt += __shfl_xor_sync(0xffffffffu, near_cnt, o);
+    if (lane == 0) {
+      if (near_cnt) atomicAdd(&near[h * 3 + 2], near_cnt);
+      atomicAdd(&counts[h * 4 + 0], selected);
+      if (selected == 0) atomicAdd(&counts[h * 4 + 1], 1);
+    }
   }
 }
 
@@ -849,7 +893,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       for (int i = 0; i < 8; ++i) {
         const int bin = 255 - (lane * 8 + i);
         c[i] = scnt[0][bin];
-        m[i] = __float2ull_rn(smass[0][bin] * kMassScale);
+        m[i] = mass_fixed(smass[0][bin]);
       }
       unsigned long long local = 0;
 #pragma unroll
@@ -1034,8 +1078,16 @@ cudaError_t init_pe_attributes() {
   cudaError_t e = cudaFuncSetAttribute(pe_prob_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kPeSmem));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pe_select_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(small_select_smem(kSmallNb)));
+  e = cudaFuncSetAttribute(pe_select_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(small_select_smem(kSmallNb)));
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_hist_ctas_per_sm, pe_hist_kernel, 256, 0);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_eqcount_ctas_per_sm, pe_eqcount_kernel,
+                                                    256, 0);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_mask_ctas_per_sm, pe_mask_kernel, 256,
+                                                       0);
 }
 
 int pe_select_launches(int nb) { return nb <= kSmallNb ? 1 : 12; }
@@ -1048,7 +1100,7 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
   const uint16_t* k = static_cast<const uint16_t*>(K);
   pe_pool_kernel<<<dim3(s.H + s.Hkv, s.nb), 128, 0, st>>>(
       q, k, w.route, s.n, s.nb, s.H, s.hq, s.hkv, s.group, s.Hkv,
-      1.4426950408889634f / sqrtf(static_cast<float>(kD)), w.qs, w.ks);
+      1.4426950408889634f / sqrtf(static_cast<float>(kD)), w.qs, w.ks, w.pe_list);
   PeProbArgs pa;
   pa.route = w.route;
   pa.nb = s.nb;
@@ -1069,19 +1121,25 @@ cudaError_t launch_pe_index(crisp_ctx ctx, const Shape& s, const crisp_cfg& cfg,
         w.pev, w.route, s.nb, s.nbw, cfg.gamma, w.rowmask, w.counts, w.near);
     return cudaGetLastError();
   }
-  pe_radix_init_kernel<<<s.H, 256, 0, st>>>(w.pe, w.hist_cnt, w.hist_mass);
+  pe_radix_init_kernel<<<s.H, 256, 0, st>>>(w.route, w.pe, w.hist_cnt, w.hist_mass,
+                                             w.pe_list);
+  // at most one CTA per item of the largest possible list (every head a PE head)
+  const int64_t items = static_cast<int64_t>(s.H) * ((s.nb + kPeRowsPerItem - 1) / kPeRowsPerItem);
+  auto resident = [&](int per_sm) {
+    return static_cast<int>(std::min<int64_t>(
+        items, static_cast<int64_t>(ctx->num_sms) * std::max(per_sm, 1)));
+  };
   for (int pass = 0; pass < 4; ++pass) {
-    const int rpc = hist_rows_per_cta(s.nb);
-    pe_hist_kernel<<<dim3((s.nb + rpc - 1) / rpc, s.H), 256, 0, st>>>(
-        w.pev, w.route, w.pe, s.nb, rpc, 24 - 8 * pass, w.hist_cnt, w.hist_mass);
+    pe_hist_kernel<<<resident(g_hist_ctas_per_sm), 256, 0, st>>>(
+        w.pev, w.pe, w.pe_list, s.nb, 24 - 8 * pass, w.hist_cnt, w.hist_mass);
     pe_digit_kernel<<<s.H, 256, 0, st>>>(w.route, pass, cfg.gamma, w.pe, w.hist_cnt,
                                          w.hist_mass);
   }
-  pe_eqcount_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, s.nb,
-                                                                w.eq_off);
+  pe_eqcount_kernel<<<resident(g_eqcount_ctas_per_sm), 256, 0, st>>>(w.pev, w.pe, w.pe_list,
+                                                                      s.nb, w.eq_off);
   pe_eqscan_kernel<<<s.H, 1024, 0, st>>>(w.route, w.pe, s.nb, w.eq_off);
-  pe_mask_kernel<<<dim3((s.nb + 7) / 8, s.H), 256, 0, st>>>(w.pev, w.route, w.pe, w.eq_off, s.nb,
-                                                            s.nbw, w.rowmask, w.counts, w.near);
+  pe_mask_kernel<<<resident(g_mask_ctas_per_sm), 256, 0, st>>>(
+      w.pev, w.pe, w.pe_list, w.eq_off, s.nb, s.nbw, w.rowmask, w.counts, w.near);
   return cudaGetLastError();
 }
 
