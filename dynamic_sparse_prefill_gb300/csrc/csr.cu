@@ -68,17 +68,30 @@ __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __
     }
     cnt[threadIdx.x] = c;
   } else {
-    for (int i = warp; i < 1024; i += 32) {
-      const int64_t row = r0 + i;
-      int c = 0;
-      if (row < rows) {
+    // A warp counts its 32 rows four at a time, every word of the four loaded before any
+    // is counted (N_b <= 8192: at most 8 words per lane and row).
+    for (int i0 = warp; i0 < 1024; i0 += 32 * 4) {
+      uint32_t wv[4][8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int64_t row = r0 + i0 + 32 * r;
+        const int nw = row < rows ? static_cast<int>(row) % nb / 32 + 1 : 0;
         const uint32_t* m = rowmask + row * nbw;
-        const int nw = static_cast<int>(row) % nb / 32 + 1;
-        for (int wd = lane; wd < nw; wd += 32) c += __popc(m[wd]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int wd = j * 32 + lane;
+          wv[r][j] = wd < nw ? m[wd] : 0u;
+        }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-      if (lane == 0) cnt[i] = c;
+      for (int r = 0; r < 4; ++r) {
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c += __popc(wv[r][j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        if (lane == 0) cnt[i0 + 32 * r] = c;
+      }
     }
   }
   __syncthreads();
@@ -147,12 +160,22 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
   __syncwarp();
   if (lane == 0) row_ptr[row] = off;
   const uint32_t* m = rowmask + row * nbw;
-  // A row whose mask holds every key block K <= I (masks have no bits above I) is written
-  // as 0..I with 16-byte stores where the offset allows: the usual row of a PE head.
   const int I = static_cast<int>(row) % nb;
   const int nw = (I >> 5) + 1;
+  // The row's mask words all load at once (N_b <= 8192: at most 8 per lane), so a row
+  // waits for one memory latency, not one per 32-word chunk.
+  constexpr int kWordsPerLane = 8;
+  uint32_t wv[kWordsPerLane];
+#pragma unroll
+  for (int j = 0; j < kWordsPerLane; ++j) {
+    const int wd = j * 32 + lane;
+    wv[j] = wd < nw ? m[wd] : 0u;
+  }
+  // A row whose mask holds every key block K <= I (masks have no bits above I) is written
+  // as 0..I with 16-byte stores where the offset allows: the usual row of a PE head.
   int cnt = 0;
-  for (int wd = lane; wd < nw; wd += 32) cnt += __popc(m[wd]);
+#pragma unroll
+  for (int j = 0; j < kWordsPerLane; ++j) cnt += __popc(wv[j]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   if (cnt == I + 1) {
@@ -169,9 +192,11 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
     return;
   }
   const uint32_t lt = (1u << lane) - 1u;
-  for (int wd0 = 0; wd0 < nw; wd0 += 32) {
-    const int wd = wd0 + lane;
-    const uint32_t bits = wd < nw ? m[wd] : 0u;
+#pragma unroll
+  for (int j = 0; j < kWordsPerLane; ++j) {
+    const int wd0 = j * 32;
+    if (wd0 >= nw) break;
+    const uint32_t bits = wv[j];
     int pre = __popc(bits);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
