@@ -551,101 +551,104 @@ __device__ __forceinline__ unsigned long long gamma_fixed(float gamma) {
   return mass_fixed(gamma);
 }
 
-// Picks the digit whose bin crosses the remaining target.  One warp per head: lane l holds
-// bins 255-8l .. 248-8l (descending), the lanes' fixed-point masses are prefix-summed by
-// shuffles, and the first lane whose bins cross the target supplies the digit (the walk
-// from the top bin down that the cumulative-coverage rule describes, with the sums grouped
-// by lane).
-__global__ void pe_digit_kernel(const uint8_t* __restrict__ route, int pass, float gamma,
-                                PeState* pe, unsigned long long* hist_cnt,
-                                unsigned long long* hist_mass) {
-  const int h = blockIdx.x;
-  if (route[h] == 0 && threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    PeState st = pe[h];
+// The digit pick of one radix pass, by all threads of a CTA (blockDim.x >= 256): thread
+// t < 256 holds bin 255 - t (count c, fixed-point mass m), so the bins run from the top
+// down with the threads.  The masses are non-negative, so the running sum from the top
+// never decreases and exactly one non-empty bin takes it from below the remaining target
+// rem to rem or above (the bin at which a walk from the top bin down stops); that bin
+// reports itself.  bin = -1: no bin reaches rem.  Ends synchronised.
+struct DigitPick {
+  unsigned long long wsum[8];  // mass per 32 bins
+  int bin;
+  unsigned long long above;    // mass of the bins above the chosen one
+  unsigned long long cnt;      // items in the chosen bin
+};
+
+__device__ void pick_crossing(int t, unsigned long long c, unsigned long long m,
+                              unsigned long long rem, DigitPick* dp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned long long incl = m;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (t < 256 && lane == 31) dp->wsum[w] = incl;
+  if (threadIdx.x == 0) dp->bin = -1;
+  __syncthreads();
+  if (t < 256) {
+    unsigned long long excl = incl - m;
+    for (int k = 0; k < w; ++k) excl += dp->wsum[k];
+    if (c && excl < rem && m >= rem - excl) {
+      dp->bin = 255 - t;
+      dp->above = excl;
+      dp->cnt = c;
+    }
+  }
+  __syncthreads();
+}
+
+// The state after a pass's digit; pass 3 also fixes the threshold and how many of the items
+// equal to it the cut takes (ceil of the remaining mass over the threshold value, at least
+// one, at most all of them).
+__device__ void finish_digit(PeState& st, int pass, float gamma, int chosen,
+                             unsigned long long above, unsigned long long cnt) {
+  const int shift = 24 - 8 * pass;
+  st.above += above;
+  st.prefix |= static_cast<uint32_t>(chosen) << shift;
+  st.decided |= 255u << shift;
+  if (pass == 3) {
+    st.thresh = st.prefix;
+    st.count_eq = cnt;
+    const double vt = static_cast<double>(__uint_as_float(st.thresh));
+    const double rem2 = static_cast<double>(gamma_fixed(gamma) - st.above) * 0x1p-56;
+    unsigned long long need = st.count_eq;
+    if (vt > 0.0) {
+      const double q = ceil(rem2 / vt);
+      need = q < 1.0 ? 1ull : static_cast<unsigned long long>(q);
+    }
+    st.need_eq = need < st.count_eq ? need : st.count_eq;
+  }
+}
+
+// Picks a pass's digit for every PE head (one CTA of 256 threads per head, thread t on bin
+// 255 - t), then clears the head's histogram for the next pass.
+__global__ void __launch_bounds__(256) pe_digit_kernel(const uint8_t* __restrict__ route,
+                                                       int pass, float gamma, PeState* pe,
+                                                       unsigned long long* hist_cnt,
+                                                       unsigned long long* hist_mass) {
+  __shared__ DigitPick dp;
+  const int h = blockIdx.x, t = threadIdx.x;
+  const unsigned long long c = hist_cnt[h * 256 + 255 - t], m = hist_mass[h * 256 + 255 - t];
+  if (route[h] == 0) {
+    PeState st = pe[h];  // the same for the whole CTA
     if (!st.select_all) {
-      const int shift = 24 - 8 * pass;
-      const unsigned long long rem = gamma_fixed(gamma) - st.above;
-      unsigned long long c[8];
-      unsigned long long m[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int bin = 255 - (lane * 8 + i);
-        c[i] = hist_cnt[h * 256 + bin];
-        m[i] = hist_mass[h * 256 + bin];
-      }
-      unsigned long long local = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (c[i]) local += m[i];
-      unsigned long long incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      unsigned long long cum = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) cum = 0;
-      int cand = -1, low = -1;
-      unsigned long long cand_cum = 0, low_m = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (!c[i]) continue;
-        const int bin = 255 - (lane * 8 + i);
-        if (cand < 0) {
-          if (cum + m[i] >= rem) {
-            cand = bin;
-            cand_cum = cum;
+      pick_crossing(t, c, m, gamma_fixed(gamma) - st.above, &dp);
+      if (t == 0) {
+        int chosen = dp.bin;
+        unsigned long long above = dp.above, cnt = dp.cnt;
+        if (chosen < 0) {
+          // no bin reaches the target (the triangle's rounded mass falls short of gamma):
+          // the first pass takes the whole triangle, a later one the lowest non-empty bin
+          unsigned long long total = 0;
+          for (int k = 0; k < 8; ++k) total += dp.wsum[k];
+          for (int bin = 0; bin < 256 && chosen < 0; ++bin)
+            if (hist_cnt[h * 256 + bin]) chosen = bin;
+          if (pass == 0 || chosen < 0) {
+            st.select_all = 1;
           } else {
-            cum += m[i];
+            above = total - hist_mass[h * 256 + chosen];
+            cnt = hist_cnt[h * 256 + chosen];
           }
         }
-        low = bin;
-        low_m = m[i];
-      }
-      int chosen = -1;
-      unsigned long long above = 0;
-      const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        chosen = __shfl_sync(0xffffffffu, cand, src);
-        above = __shfl_sync(0xffffffffu, cand_cum, src);
-      } else {
-        const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
-        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
-        if (pass == 0 || any == 0) {
-          st.select_all = 1;  // the whole triangle holds less than gamma
-        } else {
-          const int src = 31 - __clz(any);
-          chosen = __shfl_sync(0xffffffffu, low, src);
-          above = total - __shfl_sync(0xffffffffu, low_m, src);
-        }
-      }
-      if (lane == 0) {
-        if (!st.select_all) {
-          st.above += above;
-          st.prefix |= static_cast<uint32_t>(chosen) << shift;
-          st.decided |= 255u << shift;
-          if (pass == 3) {
-            st.thresh = st.prefix;
-            st.count_eq = hist_cnt[h * 256 + chosen];
-            const double vt = static_cast<double>(__uint_as_float(st.thresh));
-            const double rem2 = static_cast<double>(gamma_fixed(gamma) - st.above) * 0x1p-56;
-            unsigned long long need = st.count_eq;
-            if (vt > 0.0) {
-              const double q = ceil(rem2 / vt);
-              need = q < 1.0 ? 1ull : static_cast<unsigned long long>(q);
-            }
-            st.need_eq = need < st.count_eq ? need : st.count_eq;
-          }
-        }
+        if (!st.select_all) finish_digit(st, pass, gamma, chosen, above, cnt);
         pe[h] = st;
       }
     }
   }
   __syncthreads();
-  hist_cnt[h * 256 + threadIdx.x] = 0;
-  hist_mass[h * 256 + threadIdx.x] = 0ull;
+  hist_cnt[h * 256 + t] = 0;
+  hist_mass[h * 256 + t] = 0ull;
 }
 
 // Number of items equal to the threshold in each PE row (for flat-order tie ranks): a warp
@@ -815,6 +818,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   __shared__ float smass[kSmallCopies][256];
   __shared__ int s_red[32];
   __shared__ PeState s_st;
+  __shared__ DigitPick s_pick;
   __shared__ int s_sel_total, s_rescued;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -870,108 +874,45 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       }
     }
     __syncthreads();
-    // the copies combined per bin (count, fp32 mass) before the fixed-point pick
+    // the copies combined per bin, thread t on bin 255 - t, then the parallel digit pick
+    unsigned long long pc = 0, pm = 0;
     if (tid < 256) {
       uint32_t cc = 0;
       float mm = 0.f;
 #pragma unroll
       for (int k = 0; k < kSmallCopies; ++k) {
-        cc += scnt[k][tid];
-        mm += smass[k][tid];
+        cc += scnt[k][255 - tid];
+        mm += smass[k][255 - tid];
       }
-      scnt[0][tid] = cc;
-      smass[0][tid] = mm;
+      pc = cc;
+      pm = mass_fixed(mm);
     }
-    __syncthreads();
-    if (warp == 0) {
-      // the digit whose bin crosses the remaining target, bins walked from the top: lane l
-      // holds bins 255 - 8l .. 248 - 8l (the same pick as pe_digit_kernel)
-      const unsigned long long rem = gamma_fixed(gamma) - st.above;
-      unsigned long long c[8];
-      unsigned long long m[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int bin = 255 - (lane * 8 + i);
-        c[i] = scnt[0][bin];
-        m[i] = mass_fixed(smass[0][bin]);
-      }
-      unsigned long long local = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (c[i]) local += m[i];
-      unsigned long long incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      unsigned long long cum = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) cum = 0;
-      int cand = -1, low = -1;
-      unsigned long long cand_cum = 0, low_m = 0;
-      unsigned long long cand_c = 0, low_c = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (!c[i]) continue;
-        const int bin = 255 - (lane * 8 + i);
-        if (cand < 0) {
-          if (cum + m[i] >= rem) {
-            cand = bin;
-            cand_cum = cum;
-            cand_c = c[i];
-          } else {
-            cum += m[i];
+    pick_crossing(tid, pc, pm, gamma_fixed(gamma) - st.above, &s_pick);
+    if (tid == 0) {
+      PeState ns = st;
+      int chosen = s_pick.bin;
+      unsigned long long above = s_pick.above, cnt = s_pick.cnt;
+      if (chosen < 0) {
+        // no bin reaches the target: as in pe_digit_kernel (the copies are still intact)
+        unsigned long long total = 0;
+        for (int k = 0; k < 8; ++k) total += s_pick.wsum[k];
+        for (int bin = 0; bin < 256 && chosen < 0; ++bin) {
+          uint32_t cc = 0;
+          float mm = 0.f;
+          for (int k = 0; k < kSmallCopies; ++k) {
+            cc += scnt[k][bin];
+            mm += smass[k][bin];
+          }
+          if (cc) {
+            chosen = bin;
+            cnt = cc;
+            above = total - mass_fixed(mm);
           }
         }
-        low = bin;
-        low_m = m[i];
-        low_c = c[i];
+        if (pass == 0 || chosen < 0) ns.select_all = 1;
       }
-      int chosen = -1;
-      unsigned long long above = 0;
-      unsigned long long chosen_c = 0;
-      bool all = false;
-      const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        chosen = __shfl_sync(0xffffffffu, cand, src);
-        above = __shfl_sync(0xffffffffu, cand_cum, src);
-        chosen_c = __shfl_sync(0xffffffffu, cand_c, src);
-      } else {
-        const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
-        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
-        if (pass == 0 || any == 0) {
-          all = true;  // the whole triangle holds less than gamma
-        } else {
-          const int src = 31 - __clz(any);
-          chosen = __shfl_sync(0xffffffffu, low, src);
-          above = total - __shfl_sync(0xffffffffu, low_m, src);
-          chosen_c = __shfl_sync(0xffffffffu, low_c, src);
-        }
-      }
-      if (lane == 0) {
-        PeState ns = st;
-        if (all) {
-          ns.select_all = 1;
-        } else {
-          ns.above += above;
-          ns.prefix |= static_cast<uint32_t>(chosen) << shift;
-          ns.decided |= 255u << shift;
-          if (pass == 3) {
-            ns.thresh = ns.prefix;
-            ns.count_eq = chosen_c;
-            const double vt = static_cast<double>(__uint_as_float(ns.thresh));
-            const double rem2 = static_cast<double>(gamma_fixed(gamma) - ns.above) * 0x1p-56;
-            unsigned long long need = ns.count_eq;
-            if (vt > 0.0) {
-              const double q = ceil(rem2 / vt);
-              need = q < 1.0 ? 1ull : static_cast<unsigned long long>(q);
-            }
-            ns.need_eq = need < ns.count_eq ? need : ns.count_eq;
-          }
-        }
-        s_st = ns;
-      }
+      if (!ns.select_all) finish_digit(ns, pass, gamma, chosen, above, cnt);
+      s_st = ns;
     }
     __syncthreads();
   }
