@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(256) pe_digit_kernel(const uint8_t* __restrict
 }
 
 // Number of items equal to the threshold in each PE row (for flat-order tie ranks): a warp
-// per row, four coalesced loads in flight per lane.
+// per row, four coalesced float4 loads in flight per lane.
 __global__ void __launch_bounds__(256) pe_eqcount_kernel(const float* __restrict__ pev,
                                                          const PeState* __restrict__ pe,
                                                          const int* __restrict__ pe_list,
@@ -668,16 +668,29 @@ __global__ void __launch_bounds__(256) pe_eqcount_kernel(const float* __restrict
     if (I >= nb) continue;
     const uint32_t* row =
         reinterpret_cast<const uint32_t*>(pev + (static_cast<size_t>(h) * nb + I) * nb);
+    const int len = I + 1;
     int c = 0;
-    for (int K0 = 0; K0 <= I; K0 += 128) {
-      uint32_t x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int K = K0 + u * 32 + lane;
-        x[u] = K <= I ? row[K] : ~st.thresh;
+    auto cnt = [&](uint32_t b) { c += b == st.thresh ? 1 : 0; };
+    if ((nb & 3) == 0) {
+      // rows start on 16-byte boundaries: four float4 loads in flight per lane
+      const uint4* row4 = reinterpret_cast<const uint4*>(row);
+      const int n4 = len >> 2;
+      int q = lane;
+      for (; q + 96 < n4; q += 128) {
+        const uint4 x = row4[q], y = row4[q + 32], z = row4[q + 64], u = row4[q + 96];
+        cnt(x.x); cnt(x.y); cnt(x.z); cnt(x.w);
+        cnt(y.x); cnt(y.y); cnt(y.z); cnt(y.w);
+        cnt(z.x); cnt(z.y); cnt(z.z); cnt(z.w);
+        cnt(u.x); cnt(u.y); cnt(u.z); cnt(u.w);
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) c += x[u] == st.thresh ? 1 : 0;
+      for (; q < n4; q += 32) {
+        const uint4 x = row4[q];
+        cnt(x.x); cnt(x.y); cnt(x.z); cnt(x.w);
+      }
+      const int K = (n4 << 2) + lane;
+      if (K < len) cnt(row[K]);
+    } else {
+      for (int K = lane; K < len; K += 32) cnt(row[K]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
@@ -716,8 +729,10 @@ __global__ void __launch_bounds__(1024) pe_eqscan_kernel(const uint8_t* __restri
 }
 
 // Row masks of PE heads: v > T, or v == T with flat rank < need; plus the diagonal.  A warp
-// per row, four 32-key words in flight per lane.  Flat-order tie ranks are needed only
-// when some but not all items equal to the threshold are taken (need_eq < count_eq).
+// per row: 128-key groups as one float4 per lane (four groups in flight) when no tie ranks
+// are needed, else four 32-key words in flight per lane with ballots in key order.
+// Flat-order tie ranks are needed only when some but not all items equal to the threshold
+// are taken (need_eq < count_eq).
 constexpr int kMaskWords = 4;
 
 __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ pev,
@@ -744,35 +759,81 @@ __global__ void __launch_bounds__(256) pe_mask_kernel(const float* __restrict__ 
     // near-threshold pairs: |v - T| <= 1e-3 T (none counted when the whole triangle is kept)
     const float T = __uint_as_float(st.thresh);
     int near_cnt = 0;
-    for (int wd0 = 0; wd0 < nw; wd0 += kMaskWords) {
-      uint32_t x[kMaskWords];
+    if (!rank_ties && (nb & 3) == 0) {
+      // Every item equal to T is kept (or the whole triangle is): 128-key groups read as one
+      // float4 per lane, four groups in flight.  Lane l holds keys 4l..4l+3 of a group, i.e.
+      // nibble l & 7 of the group's word l >> 3; three xor shuffles OR the eight nibbles of
+      // each word together.
+      const float4* row4 = reinterpret_cast<const float4*>(row);
+      const int ng = (I >> 7) + 1;  // groups holding keys K <= I
+      for (int g0 = 0; g0 < ng; g0 += 4) {
+        float4 x[4];
 #pragma unroll
-      for (int u = 0; u < kMaskWords; ++u) {
-        const int K = (wd0 + u) * 32 + lane;
-        x[u] = K <= I ? __float_as_uint(row[K]) : 0u;
-      }
+        for (int u = 0; u < 4; ++u) {
+          const int g = g0 + u;
+          x[u] = (g < ng && g * 128 + 4 * lane <= I) ? row4[g * 32 + lane]
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-      for (int u = 0; u < kMaskWords; ++u) {
-        const int wd = wd0 + u;
-        if (wd >= nw) break;
-        const bool valid = wd * 32 + lane <= I;
-        bool sel = valid && (all || x[u] > st.thresh);
-        near_cnt += (valid && !all && fabsf(__uint_as_float(x[u]) - T) <= 1e-3f * T) ? 1 : 0;
-        if (!all) {
-          const bool eq = valid && x[u] == st.thresh;
-          if (rank_ties) {
-            const unsigned beq = __ballot_sync(0xffffffffu, eq);
-            const int64_t rank = eq_base + __popc(beq & ((1u << lane) - 1u));
-            sel = sel || (eq && rank < static_cast<int64_t>(st.need_eq));
-            eq_base += __popc(beq);
-          } else {
-            sel = sel || eq;
+        for (int u = 0; u < 4; ++u) {
+          const int g = g0 + u;
+          if (g >= ng) break;
+          const int K0 = g * 128 + 4 * lane;
+          const float xe[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+          uint32_t nib = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const bool valid = K0 + e <= I;
+            const uint32_t b = __float_as_uint(xe[e]);
+            nib |= (valid && (all || b >= st.thresh)) ? (1u << e) : 0u;
+            near_cnt += (valid && !all && fabsf(xe[e] - T) <= 1e-3f * T) ? 1 : 0;
+          }
+          selected += __popc(nib);
+          uint32_t word = nib << (4 * (lane & 7));
+          word |= __shfl_xor_sync(0xffffffffu, word, 1);
+          word |= __shfl_xor_sync(0xffffffffu, word, 2);
+          word |= __shfl_xor_sync(0xffffffffu, word, 4);
+          const int wd = g * 4 + (lane >> 3);
+          if ((lane & 7) == 0 && wd < nw) {
+            if (wd == (I >> 5)) word |= 1u << (I & 31);
+            mrow[wd] = word;
           }
         }
-        unsigned word = __ballot_sync(0xffffffffu, sel);
-        selected += __popc(word);
-        if (wd == (I >> 5)) word |= 1u << (I & 31);
-        if (lane == 0) mrow[wd] = word;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) selected += __shfl_xor_sync(0xffffffffu, selected, o);
+    } else {
+      // tie ranks (or rows not 16-byte aligned): a 32-key word per step, ballots in key order
+      for (int wd0 = 0; wd0 < nw; wd0 += kMaskWords) {
+        uint32_t x[kMaskWords];
+#pragma unroll
+        for (int u = 0; u < kMaskWords; ++u) {
+          const int K = (wd0 + u) * 32 + lane;
+          x[u] = K <= I ? __float_as_uint(row[K]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kMaskWords; ++u) {
+          const int wd = wd0 + u;
+          if (wd >= nw) break;
+          const bool valid = wd * 32 + lane <= I;
+          bool sel = valid && (all || x[u] > st.thresh);
+          near_cnt += (valid && !all && fabsf(__uint_as_float(x[u]) - T) <= 1e-3f * T) ? 1 : 0;
+          if (!all) {
+            const bool eq = valid && x[u] == st.thresh;
+            if (rank_ties) {
+              const unsigned beq = __ballot_sync(0xffffffffu, eq);
+              const int64_t rank = eq_base + __popc(beq & ((1u << lane) - 1u));
+              sel = sel || (eq && rank < static_cast<int64_t>(st.need_eq));
+              eq_base += __popc(beq);
+            } else {
+              sel = sel || eq;
+            }
+          }
+          unsigned word = __ballot_sync(0xffffffffu, sel);
+          selected += __popc(word);
+          if (wd == (I >> 5)) word |= 1u << (I & 31);
+          if (lane == 0) mrow[wd] = word;
+        }
       }
     }
 #pragma unroll
