@@ -620,3 +620,62 @@ def test_batch_two_matches_flattened_heads(dsp):
     for key in ("route_vs", "c_struct", "sel_v", "sel_s", "row_ptr", "col"):
         assert np.array_equal(sels[0][key], sels[1][key]), key
     assert torch.equal(outs[0], outs[1])
+
+
+def test_batch_two_matches_flattened_heads_multi_kernel(dsp):
+    """The same check at 64k (N_b = 512, above the one-CTA limit): the PE radix passes, tie
+    counts and masks walk the device-built list of PE heads, which with batch = 2 holds heads
+    of both entries; routes, selections and outputs must match the flattened layout bit for
+    bit, and the flattened case holds sampled oracle parity."""
+    w = Workload("batch_flat_64k", n=65536, hq=8, hkv=4, seed=78, pe_heads=(1, 6),
+                 needles=("uniform", 2, 6))
+    g = generate(w)
+    run_parity(dsp, w, g, sample=(4, 6), seed=3)
+    q, k, v = to_device(g["q"]), to_device(g["k"]), to_device(g["v"])
+    outs, sels = [], []
+    for dims in (dsp.make_dims(1, w.n, 8, 4), dsp.make_dims(2, w.n, 4, 2)):
+        ctx = dsp.Context(dims)
+        o = torch.empty_like(q)
+        ctx.prefill(dims, q, k, v, _cfg(dsp, w), o)
+        assert ctx.sync_status() == 0
+        sels.append(ctx.selection_get(dims))
+        outs.append(o.clone())
+        ctx.close()
+    assert sels[0]["route_vs"].tolist().count(0) == 2  # one PE head in each batch entry
+    for key in ("route_vs", "c_struct", "sel_v", "sel_s", "row_ptr", "col"):
+        assert np.array_equal(sels[0][key], sels[1][key]), key
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_repeated_selections_reset_their_state(dsp):
+    """One context, selections with different PE head sets in a row at 64k (the multi-kernel
+    PE path): every head forced PE, the planted routes, every head forced VS, the planted
+    routes again.  Each must equal what a fresh context selects on the same inputs bit for
+    bit: the PE head list, the radix state, the histograms and the near counts are rebuilt
+    on every call."""
+    w = Workload("repeat_64k", n=65536, hq=8, hkv=4, seed=79, pe_heads=(2, 5),
+                 needles=("uniform", 2, 6))
+    g = generate(w)
+    q, k = to_device(g["q"]), to_device(g["k"])
+    dims = dsp.make_dims(1, w.n, w.hq, w.hkv)
+    keys = ("route_vs", "c_struct", "sel_v", "sel_s", "counts", "row_ptr", "col")
+
+    def fresh(flags):
+        c = dsp.Context(dims)
+        c.select(dims, q, k, _cfg(dsp, w, flags=flags))
+        assert c.sync_status() == 0
+        out = c.selection_get(dims), c.stats(dims)
+        c.close()
+        return out
+
+    ref = {f: fresh(f) for f in (dsp.FLAG_FORCE_PE, 0, dsp.FLAG_FORCE_VS)}
+    ctx = dsp.Context(dims)
+    for flags in (dsp.FLAG_FORCE_PE, 0, dsp.FLAG_FORCE_VS, 0):
+        ctx.select(dims, q, k, _cfg(dsp, w, flags=flags))
+        assert ctx.sync_status() == 0
+        sel, st = ctx.selection_get(dims), ctx.stats(dims)
+        rsel, rst = ref[flags]
+        for key in keys:
+            assert np.array_equal(sel[key], rsel[key]), (flags, key)
+        assert st == rst, flags
+    ctx.close()
