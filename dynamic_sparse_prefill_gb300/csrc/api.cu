@@ -500,7 +500,7 @@ int32_t crisp_prefill_launches(const crisp_dims* dims, int32_t num_sms) {
   const Shape s = make_shape(*dims);
   const int per = attention_kv_heads_per_launch(s, num_sms);
   // selection: PatSearch and route, PE block means 1, pooled softmax 1, the gamma cut, CSR 4
-  return patsearch_launches(s.nb) + 1 + 1 + pe_select_launches(s.nb) + 4 +
+  return patsearch_launches(s.nb) + 1 + 1 + pe_select_launches(s.nb) + 3 +
          order_launches(s, num_sms) + (s.Hkv + per - 1) / per + 1;
 }
 

@@ -5,53 +5,42 @@
 // tables" returns S_v u S_s u {0, N_b-1}; "Prerequisites" defines the mask M_S of
 // A(Q,K,V,S).  For a VS head, query block I keeps key block K <= I when K is a selected
 // vertical block, when I-K is a selected slash block, when K = 0 (sink) or K = I (local
-// window, the diagonal).  PE rows come from pe_index.cu.  Rows are stored as bitmasks
-// over key blocks, then compacted into CSR with ascending key blocks.
+// window, the diagonal).  PE rows come from pe_index.cu as bitmasks over key blocks; VS
+// rows are computed word by word from the head's S_v and S_s bit words where they are
+// counted and compacted into CSR with ascending key blocks.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace crisp {
 namespace {
 
-constexpr int kRowsPerCta = 32;
-
-// Row masks of a VS head, one 32-key word per thread.  The route kernel wrote the vertical
-// selection and the slash selection reversed (bit x = sels[N_b-1-x]) as bit arrays; for
-// query block I, key K <= I is a slash key iff sels[I-K], i.e. bit N_b-1-I+K of the
-// reversed array, so a row word is a 64-bit funnel shift of that array.  Every row-mask
-// writer sets no bit above the diagonal and every reader stops at the diagonal's word
-// ((I >> 5) + 1 words for query block I), so the words past it are left unwritten.
-__global__ void __launch_bounds__(256) vs_rowmask_kernel(const uint8_t* __restrict__ route,
-                                                         const uint32_t* __restrict__ selbits,
-                                                         int nb, int nbw, uint32_t* rowmask) {
-  extern __shared__ uint32_t sbits[];  // [nbw] vertical, [nbw + 1] reversed slash
-  const int h = blockIdx.y;
-  if (!route[h]) return;
-  const uint32_t* src = selbits + static_cast<size_t>(h) * (2 * nbw + 1);
-  for (int i = threadIdx.x; i < 2 * nbw + 1; i += blockDim.x) sbits[i] = src[i];
-  __syncthreads();
-  const uint32_t* sv = sbits;
-  const uint32_t* sr = sbits + nbw;
-  const int I0 = blockIdx.x * kRowsPerCta;
-  const int nrows = min(kRowsPerCta, nb - I0);
-  for (int idx = threadIdx.x; idx < nrows * nbw; idx += blockDim.x) {
-    const int I = I0 + idx / nbw, wd = idx % nbw;
-    const int K0 = wd * 32;
-    if (K0 > I) continue;  // words past the diagonal's are neither written nor read
-    const int sh = nb - 1 - I + K0;  // bit of the reversed array for K = K0 (<= nb - 1)
-    uint32_t out = sv[wd] | __funnelshift_r(sr[sh >> 5], sr[(sh >> 5) + 1], sh & 31);
-    if (wd == 0) out |= 1u;  // the sink block
-    const int top = I - K0;  // bits 0..top are keys K <= I
-    if (top < 31) out &= (2u << top) - 1u;
-    if (top < 32) out |= 1u << top;  // the diagonal block
-    rowmask[(static_cast<size_t>(h) * nb + I) * nbw + wd] = out;
-  }
+// A 32-key word of query block I's key set.  VS heads: computed from the head's bit words
+// (written once by the route kernel: S_v in block order, then S_s reversed, bit x =
+// sels[N_b-1-x]); for query block I, key K <= I is a slash key iff sels[I-K], i.e. bit
+// N_b-1-I+K of the reversed array, so a word is a 64-bit funnel shift of that array, plus
+// the sink block 0 and the diagonal I.  PE heads: the mask pe_index.cu wrote.  No word has
+// a bit above the diagonal, and no caller asks for a word past the diagonal's ((I >> 5) + 1
+// words for query block I).
+__device__ __forceinline__ uint32_t row_word(bool vs, const uint32_t* __restrict__ sb,
+                                             const uint32_t* __restrict__ m, int nb, int nbw,
+                                             int I, int wd) {
+  if (!vs) return m[wd];
+  const int K0 = wd * 32;
+  const int sh = nb - 1 - I + K0;  // bit of the reversed array for K = K0 (<= nb - 1)
+  uint32_t out = sb[wd] | __funnelshift_r(sb[nbw + (sh >> 5)], sb[nbw + (sh >> 5) + 1], sh & 31);
+  if (wd == 0) out |= 1u;  // the sink block
+  const int top = I - K0;  // bits 0..top are keys K <= I
+  if (top < 31) out &= (2u << top) - 1u;
+  if (top < 32) out |= 1u << top;  // the diagonal block
+  return out;
 }
 
 // Counts the blocks of 1024 rows (a warp per row, or a thread per row when a row mask is
 // at most 16 words) and scans them inside the CTA: row_ptr[row] = offset within the CTA's
 // rows, blk[b] = the CTA's total.
-__global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __restrict__ rowmask,
+__global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint8_t* __restrict__ route,
+                                                              const uint32_t* __restrict__ selbits,
+                                                              const uint32_t* __restrict__ rowmask,
                                                               int64_t rows, int nb, int nbw,
                                                               int64_t* row_ptr, int64_t* blk) {
   __shared__ int cnt[1024];
@@ -62,9 +51,12 @@ __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __
     const int64_t row = r0 + threadIdx.x;
     int c = 0;
     if (row < rows) {
+      const int h = static_cast<int>(row) / nb, I = static_cast<int>(row) % nb;
+      const bool vs = route[h] != 0;
+      const uint32_t* sb = selbits + static_cast<size_t>(h) * (2 * nbw + 1);
       const uint32_t* m = rowmask + row * nbw;
-      const int nw = static_cast<int>(row) % nb / 32 + 1;
-      for (int wd = 0; wd < nw; ++wd) c += __popc(m[wd]);
+      const int nw = I / 32 + 1;
+      for (int wd = 0; wd < nw; ++wd) c += __popc(row_word(vs, sb, m, nb, nbw, I, wd));
     }
     cnt[threadIdx.x] = c;
   } else {
@@ -75,12 +67,15 @@ __global__ void __launch_bounds__(1024) csr_count_scan_kernel(const uint32_t* __
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int64_t row = r0 + i0 + 32 * r;
-        const int nw = row < rows ? static_cast<int>(row) % nb / 32 + 1 : 0;
+        const int h = static_cast<int>(row) / nb, I = static_cast<int>(row) % nb;
+        const int nw = row < rows ? I / 32 + 1 : 0;
+        const bool vs = row < rows && route[h] != 0;
+        const uint32_t* sb = selbits + static_cast<size_t>(h) * (2 * nbw + 1);
         const uint32_t* m = rowmask + row * nbw;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int wd = j * 32 + lane;
-          wv[r][j] = wd < nw ? m[wd] : 0u;
+          wv[r][j] = wd < nw ? row_word(vs, sb, m, nb, nbw, I, wd) : 0u;
         }
       }
 #pragma unroll
@@ -148,7 +143,9 @@ __global__ void __launch_bounds__(1024) csr_blk_scan_kernel(int64_t* blk, int nb
 // Finishes row_ptr (adds the CTA offset of the scan).  Lanes load 32 words at a time; then
 // the warp walks the nonzero ones, every lane writing the index of its bit if set, so each
 // word's entries are stored by consecutive lanes to consecutive addresses.
-__global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restrict__ rowmask,
+__global__ void __launch_bounds__(256) csr_fill_kernel(const uint8_t* __restrict__ route,
+                                                       const uint32_t* __restrict__ selbits,
+                                                       const uint32_t* __restrict__ rowmask,
                                                        int64_t* row_ptr,
                                                        const int64_t* __restrict__ blk,
                                                        int64_t rows, int nb, int nbw,
@@ -160,8 +157,10 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
   __syncwarp();
   if (lane == 0) row_ptr[row] = off;
   const uint32_t* m = rowmask + row * nbw;
-  const int I = static_cast<int>(row) % nb;
+  const int h = static_cast<int>(row) / nb, I = static_cast<int>(row) % nb;
   const int nw = (I >> 5) + 1;
+  const bool vs = route[h] != 0;
+  const uint32_t* sb = selbits + static_cast<size_t>(h) * (2 * nbw + 1);
   // The row's mask words all load at once (N_b <= 8192: at most 8 per lane), so a row
   // waits for one memory latency, not one per 32-word chunk.
   constexpr int kWordsPerLane = 8;
@@ -169,7 +168,7 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
 #pragma unroll
   for (int j = 0; j < kWordsPerLane; ++j) {
     const int wd = j * 32 + lane;
-    wv[j] = wd < nw ? m[wd] : 0u;
+    wv[j] = wd < nw ? row_word(vs, sb, m, nb, nbw, I, wd) : 0u;
   }
   // A row whose mask holds every key block K <= I (masks have no bits above I) is written
   // as 0..I with 16-byte stores where the offset allows: the usual row of a PE head.
@@ -220,17 +219,13 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint32_t* __restric
 
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st) {
   Workspace& w = ctx->ws;
-  vs_rowmask_kernel<<<dim3((s.nb + kRowsPerCta - 1) / kRowsPerCta, s.H), 256,
-                      sizeof(uint32_t) * (2 * s.nbw + 1), st>>>(w.route, w.selbits, s.nb, s.nbw,
-                                                                 w.rowmask);
   const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
   const int nblk = static_cast<int>((rows + 1023) / 1024);
-  csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.rowmask, rows, s.nb, s.nbw, w.row_ptr,
-                                                w.scan_blk);
+  csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.route, w.selbits, w.rowmask, rows, s.nb, s.nbw,
+                                                w.row_ptr, w.scan_blk);
   csr_blk_scan_kernel<<<1, 1024, 0, st>>>(w.scan_blk, nblk, rows, w.row_ptr);
-  csr_fill_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(w.rowmask, w.row_ptr,
-                                                                        w.scan_blk, rows, s.nb,
-                                                                        s.nbw, w.col);
+  csr_fill_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+      w.route, w.selbits, w.rowmask, w.row_ptr, w.scan_blk, rows, s.nb, s.nbw, w.col);
   return cudaGetLastError();
 }
 
