@@ -499,8 +499,9 @@ int32_t crisp_prefill_launches(const crisp_dims* dims, int32_t num_sms) {
   if (!dims || num_sms < 1 || check_dims(dims) != CRISP_OK) return 0;
   const Shape s = make_shape(*dims);
   const int per = attention_kv_heads_per_launch(s, num_sms);
-  // selection: PatSearch and route, PE block means 1, pooled softmax 1, the gamma cut, CSR 4
-  return patsearch_launches(s.nb) + 1 + 1 + pe_select_launches(s.nb) + 3 +
+  // selection: PatSearch and route, PE block means 1, pooled softmax 1, the gamma cut, CSR
+  return patsearch_launches(s.nb) + 1 + 1 + pe_select_launches(s.nb) +
+         csr_launches(static_cast<int64_t>(s.H) * s.nb) +
          order_launches(s, num_sms) + (s.Hkv + per - 1) / per + 1;
 }
 

@@ -149,11 +149,22 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint8_t* __restrict
                                                        int64_t* row_ptr,
                                                        const int64_t* __restrict__ blk,
                                                        int64_t rows, int nb, int nbw,
-                                                       int32_t* col) {
+                                                       int raw_blk, int32_t* col) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
-  int64_t off = row_ptr[row] + blk[row >> 10];
+  // raw_blk: blk holds each 1024-row block's total, not yet scanned (at most 32 blocks):
+  // the row's base is the sum of the totals of the blocks before its own.
+  int64_t base;
+  if (raw_blk) {
+    int64_t x = lane < static_cast<int>(row >> 10) ? blk[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    base = x;
+  } else {
+    base = blk[row >> 10];
+  }
+  int64_t off = row_ptr[row] + base;
   __syncwarp();
   if (lane == 0) row_ptr[row] = off;
   const uint32_t* m = rowmask + row * nbw;
@@ -177,6 +188,7 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint8_t* __restrict
   for (int j = 0; j < kWordsPerLane; ++j) cnt += __popc(wv[j]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (raw_blk && row == rows - 1 && lane == 0) row_ptr[rows] = off + cnt;  // nnz
   if (cnt == I + 1) {
     const int mis = static_cast<int>((4 - (off & 3)) & 3);  // elements before a 16-byte boundary
     const int head = mis < I + 1 ? mis : I + 1;
@@ -217,15 +229,21 @@ __global__ void __launch_bounds__(256) csr_fill_kernel(const uint8_t* __restrict
 
 }  // namespace
 
+bool csr_raw_blocks(int64_t rows) { return (rows + 1023) / 1024 <= 32; }
+
+int csr_launches(int64_t rows) { return csr_raw_blocks(rows) ? 2 : 3; }
+
 cudaError_t launch_build_csr(crisp_ctx ctx, const Shape& s, cudaStream_t st) {
   Workspace& w = ctx->ws;
   const int64_t rows = static_cast<int64_t>(s.H) * s.nb;
   const int nblk = static_cast<int>((rows + 1023) / 1024);
   csr_count_scan_kernel<<<nblk, 1024, 0, st>>>(w.route, w.selbits, w.rowmask, rows, s.nb, s.nbw,
                                                 w.row_ptr, w.scan_blk);
-  csr_blk_scan_kernel<<<1, 1024, 0, st>>>(w.scan_blk, nblk, rows, w.row_ptr);
+  // Up to 32 blocks of rows the fill kernel sums the block totals itself (one launch fewer).
+  const int raw_blk = csr_raw_blocks(rows) ? 1 : 0;
+  if (!raw_blk) csr_blk_scan_kernel<<<1, 1024, 0, st>>>(w.scan_blk, nblk, rows, w.row_ptr);
   csr_fill_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-      w.route, w.selbits, w.rowmask, w.row_ptr, w.scan_blk, rows, s.nb, s.nbw, w.col);
+      w.route, w.selbits, w.rowmask, w.row_ptr, w.scan_blk, rows, s.nb, s.nbw, raw_blk, w.col);
   return cudaGetLastError();
 }
 

@@ -186,6 +186,7 @@ int pe_select_launches(int nb);
 int attention_kv_heads_per_launch(const Shape& s, int num_sms);
 // Launches of the attention work order (1 for short sequences, else 3).
 int order_launches(const Shape& s, int num_sms);
+int csr_launches(int64_t rows);
 // tmQ/tmK/tmV: 3-D maps of Q, K, V (dims {64, rows, 2}, box {64, 128, 2}; see make_map3).
 cudaError_t launch_attention(crisp_ctx ctx, const Shape& s, const CUtensorMap& tmQ,
                              const CUtensorMap& tmK, const CUtensorMap& tmV, void* O, bool dense,

@@ -222,10 +222,11 @@ crisp_status crisp_jsd(crisp_ctx ctx, const crisp_dims* dims, const void* Q, con
 crisp_status crisp_attend_info(crisp_ctx ctx, void* stream, int64_t* rows);
 
 /* Number of kernel launches one crisp_prefill enqueues for `dims` on a GPU with `num_sms`
- * SMs: selection 8 for N_b = n/128 <= 256, else 21 (PatSearch and the route 2 or 4;
- * PEIndex: block means 1, pooled softmax 1, the gamma cut 1 or 12; CSR 3), the attention
- * work order (1 for at most 16384 query-block rows, else 3), the fast attention kernel
- * once per group of KV heads, and the rescue pass once.  Host-only arithmetic (no context, no CUDA call); 0 for dims
+ * SMs: selection 7 for N_b = n/128 <= 256, else 20 or 21 (PatSearch and the route 2 or
+ * 4; PEIndex: block means 1, pooled softmax 1, the gamma cut 1 or 12; CSR 2 for at most
+ * 32768 query-block rows over all heads, else 3), the attention work order (1 for at most
+ * 16384 query-block rows, else 3), the fast attention kernel once per group of KV heads,
+ * and the rescue pass once.  Host-only arithmetic (no context, no CUDA call); 0 for dims
  * the library does not support. */
 int32_t crisp_prefill_launches(const crisp_dims* dims, int32_t num_sms);
 

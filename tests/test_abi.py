@@ -35,17 +35,19 @@ def test_prefill_launch_plan(L):
     """Launches per crisp_prefill on 152 SMs.  Selection: PatSearch and the route (2 for
     N_b <= 256, where the route kernel merges the row statistics itself, else 4), PE block
     means 1, pooled softmax 1, the gamma cut (1 kernel for N_b <= 256, else 12: radix init,
-    four histogram and digit passes, tie counts and scan, masks), CSR 3.  Then the work order (1
+    four histogram and digit passes, tie counts and scan, masks), CSR 2 for at most 32768
+    rows (else 3).  Then the work order (1
     kernel for at most 16384 rows, else 3), the attention launches (KV heads per launch:
     >= 8 rows per SM, or as many as fit 48 MB of L2) and the rescue pass."""
     lib = L.lib()
     cases = [((1, 524288, 32, 8), 21 + 3 + 8 + 1),    # one KV head per launch
-             ((1, 131072, 32, 8), 21 + 3 + 8 + 1),
-             ((1, 32768, 32, 8), 8 + 1 + 3 + 1),      # N_b = 256: the short-sequence kernels
-             ((1, 32896, 32, 8), 21 + 1 + 4 + 1),     # N_b = 257 (2 KV heads per launch)
-             ((1, 8192, 32, 8), 8 + 1 + 1 + 1),       # everything in one attention launch
-             ((1, 4096, 2, 2), 8 + 1 + 1 + 1),
-             ((2, 16384, 32, 8), 8 + 1 + 3 + 1)]     # 16 KV heads, 6 per launch (8 MiB each)
+             ((1, 131072, 32, 8), 20 + 3 + 8 + 1),    # 32768 rows: CSR in 2 launches
+             ((1, 131200, 32, 8), 21 + 3 + 8 + 1),    # 32800 rows: CSR in 3
+             ((1, 32768, 32, 8), 7 + 1 + 3 + 1),      # N_b = 256: the short-sequence kernels
+             ((1, 32896, 32, 8), 20 + 1 + 4 + 1),     # N_b = 257 (2 KV heads per launch)
+             ((1, 8192, 32, 8), 7 + 1 + 1 + 1),       # everything in one attention launch
+             ((1, 4096, 2, 2), 7 + 1 + 1 + 1),
+             ((2, 16384, 32, 8), 7 + 1 + 3 + 1)]     # 16 KV heads, 6 per launch (8 MiB each)
     for (b, n, hq, hkv), want in cases:
         d = L.make_dims(b, n, hq, hkv)
         assert lib.crisp_prefill_launches(ctypes.byref(d), 152) == want, (b, n, hq, hkv)
