@@ -164,6 +164,8 @@ struct AttnArgs {
 struct Item {
   int h, I, hk, L;
   int64_t beg;
+  int diag;  // the row's last block is its diagonal (fast pass; only it can be: rows are
+             // strictly ascending within [0, I])
 };
 
 // Item at position ke of the launch's order: a listed row (rescue pass), a row of the
@@ -304,28 +306,46 @@ __device__ __forceinline__ void produce_v(const AttnArgs& a, int num_items, cons
 constexpr int kItemRing = 4;
 constexpr int kItemReaders = 11;  // V producer, S issuer, P.V issuer, 8 softmax warps
 
+// A ring slot: the item's position in the launch's order and the item decoded by the
+// producer (the readers then need no global loads to start it).
+struct FeedItem {
+  int k, h, I, hk, L, diag;
+  long long beg;
+};
+
 struct ItemFeed {
-  volatile int* slot;
+  volatile FeedItem* slot;
   uint64_t* full;   // [kItemRing] count 1
   uint64_t* empty;  // [kItemRing] count kItemReaders
 };
 
+__device__ __forceinline__ int read_slot(volatile FeedItem* e, Item& it) {
+  it.h = e->h;
+  it.I = e->I;
+  it.hk = e->hk;
+  it.L = e->L;
+  it.diag = e->diag;
+  it.beg = e->beg;
+  return e->k;
+}
+
 // One thread: the idx-th item of the stream (-1: end), or -2 if a wait ran out.
-__device__ __forceinline__ int feed_next(const ItemFeed& f, int idx, uint32_t* err,
+__device__ __forceinline__ int feed_next(const ItemFeed& f, int idx, Item& it, uint32_t* err,
                                          volatile int* abort_flag, uint64_t tmo) {
   const int s = idx % kItemRing;
   if (!mbar_wait(&f.full[s], (idx / kItemRing) & 1, err, abort_flag, tmo)) return -2;
-  const int k = f.slot[s];
+  const int k = read_slot(&f.slot[s], it);
   mbar_arrive(&f.empty[s]);
   return k;
 }
 
 // A whole warp: the same, one release per warp.
-__device__ __forceinline__ int feed_next_warp(const ItemFeed& f, int idx, uint32_t* err,
-                                              volatile int* abort_flag, uint64_t tmo) {
+__device__ __forceinline__ int feed_next_warp(const ItemFeed& f, int idx, Item& it,
+                                              uint32_t* err, volatile int* abort_flag,
+                                              uint64_t tmo) {
   const int s = idx % kItemRing;
   if (!warp_wait(&f.full[s], (idx / kItemRing) & 1, err, abort_flag, tmo)) return -2;
-  const int k = f.slot[s];
+  const int k = read_slot(&f.slot[s], it);
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&f.empty[s]);
   return k;
@@ -351,10 +371,21 @@ __device__ __forceinline__ void produce_qk_feed(const AttnArgs& a, int num_items
       break;
     int k = atomicAdd(a.work_ctr, 1);
     if (k >= num_items) k = -1;
-    feed.slot[s] = k;
+    Item it{};
+    if (k >= 0) {
+      it = item_of(a, a.item_base + k);
+      it.diag = it.L > 0 && block_of(a, it, it.L - 1) == it.I ? 1 : 0;
+    }
+    volatile FeedItem* e = &feed.slot[s];
+    e->h = it.h;
+    e->I = it.I;
+    e->hk = it.hk;
+    e->L = it.L;
+    e->diag = it.diag;
+    e->beg = it.beg;
+    e->k = k;
     mbar_arrive(&feed.full[s]);
     if (k < 0) break;
-    const Item it = item_of(a, a.item_base + k);
     if (item_idx > 0 && !mbar_wait(q_empty, (item_idx - 1) & 1, a.err, abort_flag, tmo)) break;
     const int qrow = it.h * a.n + it.I * kBlk;
     mbar_arrive_expect_tx(q_full, kTileBytes);
@@ -391,9 +422,9 @@ __device__ __forceinline__ void produce_v_feed(const AttnArgs& a, const CUtensor
   int gv = 0;
   bool ok = true;
   for (int item_idx = 0; ok; ++item_idx) {
-    const int k = feed_next(feed, item_idx, a.err, abort_flag, tmo);
+    Item it;
+    const int k = feed_next(feed, item_idx, it, a.err, abort_flag, tmo);
     if (k < 0) break;
-    const Item it = item_of(a, a.item_base + k);
     for (int j = 0; j < it.L; ++j) {
       int kb = block_of(a, it, j);
       if (kb < 0 || kb > it.I) kb = it.I;
@@ -746,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* feed_empty = feed_full + kItemRing;  // [kItemRing]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(feed_empty + kItemRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const ItemFeed feed{reinterpret_cast<volatile int*>(tmem_slot + 2), feed_full, feed_empty};
+  const ItemFeed feed{reinterpret_cast<volatile FeedItem*>(tmem_slot + 2), feed_full, feed_empty};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns;
@@ -812,9 +843,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int gk = 0, item_idx = 0;
         bool ok = true;
         for (; ok; ++item_idx) {
-          const int kf = feed_next(feed, item_idx, a.err, abort_flag, tmo);
+          Item it;
+          const int kf = feed_next(feed, item_idx, it, a.err, abort_flag, tmo);
           if (kf < 0) break;
-          const Item it = item_of(a, a.item_base + kf);
           if (!mbar_wait(q_full, item_idx & 1, a.err, abort_flag, tmo)) {
             ok = false;
             break;
@@ -853,9 +884,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int gv = 0, item_idx = 0;
         bool ok = true;
         for (; ok; ++item_idx) {
-          const int kf = feed_next(feed, item_idx, a.err, abort_flag, tmo);
+          Item it;
+          const int kf = feed_next(feed, item_idx, it, a.err, abort_flag, tmo);
           if (kf < 0) break;
-          const Item it = item_of(a, a.item_base + kf);
           for (int j = 0; j < it.L; ++j) {
             const int t = gv & 1;
             const int s = gv % kFastVStages;  // == t
@@ -909,9 +940,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     for (; ok; ++item_idx) {
-      const int kf = feed_next_warp(feed, item_idx, a.err, abort_flag, tmo);
+      Item it;
+      const int kf = feed_next_warp(feed, item_idx, it, a.err, abort_flag, tmo);
       if (kf < 0) break;
-      const Item it = item_of(a, a.item_base + kf);
       const int j0 = (t ^ gbase) & 1;  // this tile's first block: (gbase + j0) & 1 == t
       // Row reference: the larger of the two tiles' first-block row maxima.
       float mfirst = -FLT_MAX;
@@ -920,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mfirst = (block_of(a, it, j0) == it.I ? row_max<true>(v, r) : row_max<false>(v, r)) *
+        mfirst = (it.diag && j0 == it.L - 1 ? row_max<true>(v, r) : row_max<false>(v, r)) *
                  a.scale_log2;
       }
       sXM[t * kBlk + r] = mfirst;
@@ -938,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const float rs = block_of(a, it, jj) == it.I ? exp_pack<true>(v, a.scale_log2, M, r)
+        const float rs = it.diag && jj == it.L - 1 ? exp_pack<true>(v, a.scale_log2, M, r)
                                                      : exp_pack<false>(v, a.scale_log2, M, r);
         ovf |= !(rs <= kOverflowSum);
         l += rs;
