@@ -24,8 +24,9 @@ namespace crisp {
 
 namespace {
 
-constexpr int kProxyThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2-9: epilogue
+constexpr int kProxyThreads = 352;  // warp 0: TMA, warps 1-2: MMA, warps 3-10: epilogue
 constexpr int kProxyStages = 4;
+static_assert(kProxyStages % 2 == 0, "each K stage must serve tiles of one parity (one MMA issuer)");
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr size_t kProxySmem = 1024 + kTileBytes * (1 + kProxyStages) + 256;
 
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -138,11 +139,16 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       for (int i = max(0, issued - kProxyStages); i < issued; ++i)
         drain_wait(&k_full[i % kProxyStages], (i / kProxyStages) & 1, a.err, tmo);
     }
-  } else if (warp == 1) {
+  } else if (warp <= 2) {
+    // Two MMA issuers, warp 1 for the even tiles (S buffer 0), warp 2 for the odd ones:
+    // tcgen05.mma issue waits for the tensor core, and after a tile's commits the issuing
+    // thread's next barrier wait lasts until that tile's MMAs are done, so one issuer leaves
+    // the tensor core idle between tiles.  With an even number of K stages every stage
+    // serves tiles of one parity, i.e. one issuer.
     if (lane == 0) {
       if (mbar_wait(q_full, 0, a.err, abort_flag, tmo)) {
         const uint32_t q_base = smem_u32(sQ);
-        for (int i = 0; i < ntiles; ++i) {
+        for (int i = warp - 1; i < ntiles; i += 2) {
           const int s = i % kProxyStages, sb = i & 1;
           if (!mbar_wait(&k_full[s], (i / kProxyStages) & 1, a.err, abort_flag, tmo)) break;
           if (i >= 2 && !mbar_wait(&s_free[sb], ((i >> 1) + 1) & 1, a.err, abort_flag, tmo))
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
     // against its running row maximum m_run and falls back to the tile's exact maximum
     // only when the sums show the tile exceeds m_run by a lot (the combine kernels accept
     // any per-tile reference maximum).
-    const int e = (warp - 2) >> 2;
+    const int e = (warp - 3) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t row_taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + e * 128;
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
     for (int i = e; i < ntiles; i += 2) {
       if (!warp_wait(&s_full[e], (i >> 1) & 1, a.err, abort_flag, tmo)) break;
       tc_fence_after();
-      // The tile's S row in one TMEM load; the buffer goes straight back to the MMA warp.
+      // The tile's S row in one TMEM load; the buffer goes straight back to its MMA issuer.
       uint32_t v[128];
       tmem_ld128(row_taddr, v);
       tc_fence_before();
