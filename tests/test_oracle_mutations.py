@@ -1,0 +1,107 @@
+"""Plants mistakes in a copy of the oracle and checks that its pins catch each one.
+
+A pin that still passes when the oracle computes something else pins nothing.  Each case
+rewrites one step of a fresh copy of oracle/crisp_oracle.py, built from its source text
+(the oracle itself is never modified), points the pin tests at the copy, and requires at
+least one of the pins named for that step to fail.  The unmodified copy must pass the
+same pins, so a broken harness cannot pass for a caught mistake.  Sections cited are those
+of the analysis page "CRISP: Cliff-awaRe Input-adaptive Sparse Prefilling with
+Structural-Mass-Motivated Routing" (paper.rainbus.top).
+"""
+import pathlib
+import types
+
+import pytest
+
+from oracle import crisp_oracle as O
+
+import tests.test_oracle_pins as pins
+
+SRC = pathlib.Path(O.__file__).read_text()
+
+
+def _copy(text):
+    mod = types.ModuleType("crisp_oracle_copy")
+    mod.__file__ = O.__file__
+    exec(compile(text, O.__file__, "exec"), mod.__dict__)
+    return mod
+
+
+def _pin(name, *args):
+    return (name, args)
+
+
+# (case, text in the oracle, replacement, pins that must catch it)
+MUTATIONS = [
+    # "Figures and tables", Algorithm 4: pooled logits scaled by 1/sqrt(d)
+    ("pe_index without 1/sqrt(d)",
+     "    logits = (qb @ kb.T) / math.sqrt(d)\n", "    logits = (qb @ kb.T)\n",
+     [_pin("test_pe_index_worked_example")]),
+    # Algorithm 4: queries pooled by block mean
+    ("pe_index pools Q by sum",
+     "    qb, kb = block_mean(q, B), block_mean(k, B)\n",
+     "    qb, kb = block_mean(q, B) * B, block_mean(k, B)\n",
+     [_pin("test_pe_index_worked_example")]),
+    # Algorithm 4: normalise by N_b
+    ("pe_index without the 1/N_b normalisation",
+     "    v_full = a_bar / nb\n", "    v_full = a_bar\n",
+     [_pin("test_pe_index_worked_example"), _pin("test_pe_scores_normalised")]),
+    # reading: an emptied query row gets its diagonal pair
+    ("pe_index without the diagonal rescue",
+     "    mask[np.arange(nb), np.arange(nb)] = True\n", "",
+     [_pin("test_pe_index_worked_example")]),
+    # "Prerequisites", JSD: a_hat is the row-averaged proxy attention pooled by key block
+    ("jsd_route on the slash score",
+     "    p_v = block_pool(vertical_score(proxy_attention(q, k, b)), B)\n",
+     "    p_v = block_pool(slash_score(proxy_attention(q, k, b)), B)\n",
+     [_pin("test_jsd_route_worked_example")]),
+    # "Prerequisites", cumulative coverage: ties of the gamma cut go to the lower index
+    ("gamma_cut ties to the higher index",
+     "    order = np.lexsort((np.arange(values.shape[0]), -values))\n",
+     "    order = np.lexsort((-np.arange(values.shape[0]), -values))\n",
+     [_pin("test_gamma_cut_bruteforce", s) for s in range(5)]
+     + [_pin("test_pe_index_worked_example")]),
+    # "Core method" step 1: the proxy softmax is causal
+    ("proxy_attention not causal",
+     "    logits[np.arange(n)[None, :] > pos[:, None]] = NEG_INF\n", "",
+     [_pin("test_proxy_uniform_logits_closed_form", 1024, 128),
+      _pin("test_slash_and_vertical_index_direction")]),
+    # Algorithm 3: the slash score indexes by query minus key position
+    ("slash_score indexed by key position",
+     "        a_s[: p + 1] += a_hat[r, p::-1]\n", "        a_s[: p + 1] += a_hat[r, : p + 1]\n",
+     [_pin("test_slash_and_vertical_index_direction"),
+      _pin("test_proxy_uniform_logits_closed_form", 1024, 128)]),
+    # Algorithm 3: the noise floor excludes the two anchor blocks
+    ("noise_floor over all blocks",
+     "    return r / (nb - 2)\n", "    return r / nb\n",
+     [_pin("test_vs_select_worked_example"), _pin("test_noise_floor_closed_form_from_c_struct")]),
+    # Algorithm 3: blocks strictly above alpha * mu
+    ("select_above_floor with >=",
+     "    c = int(np.count_nonzero(p > alpha * mu))\n",
+     "    c = int(np.count_nonzero(p >= alpha * mu))\n",
+     [_pin("test_vs_select_threshold_is_strict"), _pin("test_vs_select_worked_example")]),
+    # "Prerequisites", A(Q,K,V,S): attention logits scaled by 1/sqrt(d)
+    ("block_sparse_attention without 1/sqrt(d)",
+     "        logits = (qi @ k[keys].T) / math.sqrt(d)\n", "        logits = (qi @ k[keys].T)\n",
+     [_pin("test_all_blocks_equals_dense_causal_sdpa", 512, 16, 128)]),
+]
+
+
+def _run(mod, pin_list, monkeypatch):
+    """Runs the pins against `mod`; returns the names of those that failed."""
+    monkeypatch.setattr(pins, "O", mod)
+    failed = []
+    for name, args in pin_list:
+        try:
+            getattr(pins, name)(*args)
+        except AssertionError:
+            failed.append(name)
+    return failed
+
+
+@pytest.mark.parametrize("case,old,new,pin_list", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(case, old, new, pin_list, monkeypatch):
+    assert SRC.count(old) == 1, f"{case}: the text to replace is not in the oracle once"
+    assert _run(_copy(SRC), pin_list, monkeypatch) == [], f"{case}: the unmodified copy fails"
+    failed = _run(_copy(SRC.replace(old, new)), pin_list, monkeypatch)
+    assert failed, f"{case}: no pin caught the planted mistake"

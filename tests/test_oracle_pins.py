@@ -218,6 +218,20 @@ def test_vs_block_mask_worked_example():
     assert rows == fx["rows"]
 
 
+def test_vs_select_threshold_is_strict():
+    """Algorithm 3 keeps the blocks strictly above alpha * mu_d.  With binary-exact scores
+    the four non-anchor blocks sit exactly on the floor (r = 1 - 1/4 - 1/4 = 1/2,
+    mu = r / 4 = 1/8, alpha = 1): only the two anchor blocks pass."""
+    p = np.array([0.25, 0.125, 0.125, 0.125, 0.125, 0.25])
+    mu = O.noise_floor(p)
+    assert mu == 0.125
+    S, c, kd = O.select_above_floor(p, 1.0, mu, 1)
+    assert (S.tolist(), c, kd) == ([0, 5], 2, 2)
+    # k_min pads with the largest remaining blocks, ties to the lower index
+    S, c, kd = O.select_above_floor(p, 1.0, mu, 3)
+    assert (S.tolist(), c, kd) == ([0, 1, 5], 2, 3)
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_vs_select_bruteforce_and_invariants(seed):
     """Brute force over all k-subsets of a tiny N_b: the selection is a maximum-mass
