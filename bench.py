@@ -449,8 +449,11 @@ def run_gpu(args, w, rank, world):
                         "the layer)",
         "algorithmic_flops_per_attend": flops,
         "traffic": None,
-        "traffic_note": "DRAM bytes are not counted in this run; they come from ncu "
-                        "captures of one attention launch at 32k tokens, scaled by units",
+        "traffic_note": "null: this run counts no DRAM bytes, and counter captures at this "
+                        "size are limited to durations. Small-case captures do not scale: one "
+                        "32k launch reads 1.33x its algorithmic bytes, one 512k launch "
+                        "(a KV head, reduced-head workload) about 7x, from L2 misses as "
+                        "its CTAs spread over the KV head's K/V",
     }
     if peak_mhz and run_mhz:
         # the measured peak was taken at its own median SM clock; scaled to this run's
