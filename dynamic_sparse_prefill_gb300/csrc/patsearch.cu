@@ -217,8 +217,8 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
               wb += sb;
             }
           } else if (c4 == q) {
-            // the warp's own chunk, split per lane without branches: selects into separate
-            // pairs of sums (the right part is dropped on the causal last tile)
+            // the warp's own chunk, split per lane by predicated adds into separate sums
+            // (the right part is dropped on the causal last tile)
             float la = 0.f, lb = 0.f, ra = 0.f, rb = 0.f;
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
@@ -226,9 +226,8 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
               ffma2(x0, x1, __uint_as_float(v[c4 * 32 + c]), __uint_as_float(v[c4 * 32 + c + 1]),
                     a.scale_log2, a.scale_log2, neg, neg);
               const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-              const bool l0 = c <= lane, l1 = c + 1 <= lane;
-              fadd2(la, lb, la, lb, l0 ? e0 : 0.f, l1 ? e1 : 0.f);
-              fadd2(ra, rb, ra, rb, l0 ? 0.f : e0, l1 ? 0.f : e1);
+              if (c <= lane) la += e0; else ra += e0;
+              if (c + 1 <= lane) lb += e1; else rb += e1;
             }
             ua += la + lb;
             if (!last) wa += ra + rb;
