@@ -80,6 +80,22 @@ MUTATIONS = [
      "    c = int(np.count_nonzero(p > alpha * mu))\n",
      "    c = int(np.count_nonzero(p >= alpha * mu))\n",
      [_pin("test_vs_select_threshold_is_strict"), _pin("test_vs_select_worked_example")]),
+    # Algorithm 2: VS iff C_struct >= tau_proxy
+    ("route with > instead of >=",
+     "    return bool(c_struct >= tau_proxy)", "    return bool(c_struct > tau_proxy)",
+     [_pin("test_route_at_threshold_is_vs")]),
+    # Algorithm 3: the floor is clamped at zero
+    ("noise_floor without the clamp at zero",
+     "    r = max(1.0 - p[0] - p[nb - 1], 0.0)", "    r = 1.0 - p[0] - p[nb - 1]",
+     [_pin("test_noise_floor_clamps_at_zero")]),
+    # reading: k_min tokens are at least ceil(k_min / B) blocks
+    ("kmin_blocks rounded down",
+     "    return -(-k_min_tokens // B)", "    return k_min_tokens // B",
+     [_pin("test_kmin_blocks")]),
+    # "Prerequisites", cumulative coverage: stop when the sum reaches gamma (>=)
+    ("gamma_cut needs the sum above gamma",
+     "    hit = np.nonzero(csum >= gamma)[0]", "    hit = np.nonzero(csum > gamma)[0]",
+     [_pin("test_gamma_cut_stops_when_the_sum_reaches_gamma")]),
     # "Prerequisites", A(Q,K,V,S): attention logits scaled by 1/sqrt(d)
     ("block_sparse_attention without 1/sqrt(d)",
      "        logits = (qi @ k[keys].T) / math.sqrt(d)\n", "        logits = (qi @ k[keys].T)\n",

@@ -232,6 +232,25 @@ def test_vs_select_threshold_is_strict():
     assert (S.tolist(), c, kd) == ([0, 1, 5], 2, 3)
 
 
+def test_noise_floor_clamps_at_zero():
+    """Algorithm 3's floor is max(1 - p_d[0] - p_d[N_b-1], 0) / (N_b - 2): when the anchor
+    blocks' scores sum past 1 (here by 2^-50, all values binary-exact) the floor is 0, and
+    blocks with score 0 are not above it."""
+    p = np.array([0.75, 0.0, 0.0, 0.25 + 2.0 ** -50])
+    assert O.noise_floor(p) == 0.0
+    S, c, kd = O.select_above_floor(p, 1.0, O.noise_floor(p), 0)
+    assert (S.tolist(), c, kd) == ([0, 3], 2, 2)
+
+
+def test_kmin_blocks():
+    """"Method step details": k_min = 1024 tokens is 8 blocks of B = 128.  Reading for
+    other values: at least k_min tokens, i.e. ceil(k_min / B) blocks."""
+    assert O.kmin_blocks(1024, 128) == 8
+    assert O.kmin_blocks(1000, 128) == 8
+    assert O.kmin_blocks(1025, 128) == 9
+    assert O.kmin_blocks(0, 128) == 0
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_vs_select_bruteforce_and_invariants(seed):
     """Brute force over all k-subsets of a tiny N_b: the selection is a maximum-mass
@@ -269,6 +288,29 @@ def test_gamma_cut_bruteforce(seed):
         assert abs(vals[sel].sum() - best) < 1e-15
         # dropping the smallest selected item falls below gamma
         assert vals[sel].sum() - vals[sel].min() < gamma
+
+
+def test_gamma_cut_stops_when_the_sum_reaches_gamma():
+    """"Prerequisites", cumulative coverage: the smallest prefix (largest first) whose sum is
+    >= gamma.  Binary-exact values reach gamma = 3/4 exactly after two items."""
+    vals = np.array([0.125, 0.5, 0.125, 0.25])
+    assert O.gamma_cut(vals, 0.75).tolist() == [1, 3]
+    assert O.gamma_cut(vals, 0.75 + 2.0 ** -40).tolist() == [0, 1, 3]
+
+
+def test_route_at_threshold_is_vs():
+    """Algorithm 2 routes a head VS iff C_struct >= tau_proxy: with tau equal to the head's
+    own C_struct the head is VS, with the next larger double it is PE."""
+    w = get("tiny_n4k")
+    g = generate(w)
+    q = O.bf16_bits_to_f64(g["q"][0])
+    k = O.bf16_bits_to_f64(g["k"][0])
+    params = O.workload_params(w)
+    c = O.crisp_select_head(q, k, **params)["c_struct"]
+    params["tau_proxy"] = c
+    assert O.crisp_select_head(q, k, **params)["route_vs"]
+    params["tau_proxy"] = float(np.nextafter(c, np.inf))
+    assert not O.crisp_select_head(q, k, **params)["route_vs"]
 
 
 def test_gamma_one_selects_everything():
