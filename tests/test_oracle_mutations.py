@@ -96,6 +96,80 @@ MUTATIONS = [
     ("gamma_cut needs the sum above gamma",
      "    hit = np.nonzero(csum >= gamma)[0]", "    hit = np.nonzero(csum > gamma)[0]",
      [_pin("test_gamma_cut_stops_when_the_sum_reaches_gamma")]),
+    # "Core method" step 1: S_anchor is the first w_sink and the last w_local keys
+    ("anchor set without the local window",
+     "    idx[max(n - w_local, 0):] = True\n", "",
+     [_pin("test_scores_sum_to_one_and_anchor_slice"),
+      _pin("test_proxy_uniform_logits_closed_form", 1024, 128)]),
+    ("anchor set without the sink",
+     "    idx[: min(w_sink, n)] = True\n", "",
+     [_pin("test_scores_sum_to_one_and_anchor_slice"),
+      _pin("test_proxy_uniform_logits_closed_form", 1024, 128)]),
+    # Algorithm 3: the vertical score is the column mean
+    ("vertical_score as a column sum",
+     "    return a_hat.sum(axis=0) / a_hat.shape[0]", "    return a_hat.sum(axis=0)",
+     [_pin("test_proxy_uniform_logits_closed_form", 1024, 128)]),
+    # reading: the diagonal mean divides by b
+    ("slash_score divided by n",
+     "    return a_s / b\n", "    return a_s / n\n",
+     [_pin("test_slash_and_vertical_index_direction"),
+      _pin("test_scores_sum_to_one_and_anchor_slice")]),
+    # reading: block pooling is a sum
+    ("block_pool as a mean",
+     "    return score.reshape(-1, B).sum(axis=1)", "    return score.reshape(-1, B).mean(axis=1)",
+     [_pin("test_mass_cliff_epsilon_closed_form", 4096, 6, 12.0),
+      _pin("test_noise_floor_closed_form_from_c_struct")]),
+    # Algorithm 3: the count is clipped to [k_min, N_b]
+    ("select_above_floor without the N_b clip",
+     "    kd = min(max(c, kmin_blocks), nb)\n    return topk_desc(p, kd), c, kd",
+     "    kd = max(c, kmin_blocks)\n    return topk_desc(p, kd), c, kd",
+     [_pin("test_vs_select_bruteforce_and_invariants", s) for s in range(6)]),
+    # reading: top-k padding ties go to the lower block index
+    ("topk_desc ties to the higher index",
+     "    order = np.lexsort((np.arange(p.shape[0]), -p))",
+     "    order = np.lexsort((-np.arange(p.shape[0]), -p))",
+     [_pin("test_vs_select_threshold_is_strict"), _pin("test_vs_select_worked_example")]),
+    # Algorithm 3: the union keeps key block 0 and the diagonal of every query block
+    ("vs_block_mask without the sink column",
+     "    m[:, 0] = True\n", "",
+     [_pin("test_vs_block_mask_worked_example")]),
+    ("vs_block_mask slash block read forward",
+     "        m[rows, rows - J] = True", "        m[rows, np.minimum(rows + J, nb - 1)] = True",
+     [_pin("test_vs_block_mask_worked_example")]),
+    # "Limitations" item 6: the median floor is over the non-anchor blocks
+    ("noise_floor_median over all blocks",
+     "    return float(np.median(p[1:nb - 1]))", "    return float(np.median(p))",
+     [_pin("test_median_floor_bruteforce", s) for s in range(4)]),
+    # Abl.1: the gamma-cumsum budget is padded to k_min
+    ("select_gamma_cumsum without k_min",
+     "    kd = min(max(cut, kmin_blocks), nb)", "    kd = cut",
+     [_pin("test_vs_variants_worked_example")]),
+    # "Algorithm 4": the PE block softmax is causal
+    ("pe_index without the causal block mask",
+     "    logits[~tri] = NEG_INF\n", "",
+     [_pin("test_pe_uniform_pooled_scores_closed_form")]),
+    # "Prerequisites", JSD: m = (x + y) / 2, logs in nats; a_bar from the last b queries
+    ("js_divergence against max(x, y)",
+     "    m = 0.5 * (x + y)", "    m = np.maximum(x, y)",
+     [_pin("test_js_divergence_closed_forms")]),
+    ("kl_divergence in bits",
+     "    return float(np.sum(x[nz] * np.log(x[nz] / y[nz])))",
+     "    return float(np.sum(x[nz] * np.log2(x[nz] / y[nz])))",
+     [_pin("test_js_divergence_closed_forms")]),
+    ("pooled_estimate over all queries",
+     "    qbar = q[n - b:].mean(axis=0)", "    qbar = q.mean(axis=0)",
+     [_pin("test_jsd_route_worked_example")]),
+    ("pooled_estimate without 1/sqrt(d)",
+     "    logits = block_mean(k, B) @ qbar / math.sqrt(d)", "    logits = block_mean(k, B) @ qbar",
+     [_pin("test_pooled_estimate_special_cases")]),
+    # "Core method" step 1: the proxy queries are the last b rows
+    ("proxy_attention on the first b rows",
+     "    q_hat = q[n - b:]", "    q_hat = q[:b]",
+     [_pin("test_jsd_route_worked_example")]),
+    # "Prerequisites", A(Q,K,V,S): token-causal inside the diagonal block
+    ("block_sparse_attention not causal inside a block",
+     "        logits[keys[None, :] > qpos[:, None]] = NEG_INF\n", "",
+     [_pin("test_all_blocks_equals_dense_causal_sdpa", 512, 16, 128)]),
     # "Prerequisites", A(Q,K,V,S): attention logits scaled by 1/sqrt(d)
     ("block_sparse_attention without 1/sqrt(d)",
      "        logits = (qi @ k[keys].T) / math.sqrt(d)\n", "        logits = (qi @ k[keys].T)\n",
