@@ -1,7 +1,14 @@
-"""CPU checks of the GPU parity helper (tests/parity.py): a selection that reproduces the
-oracle's passes, and each kind of mistake the helper exists to catch is rejected -- a
-changed CSR row of a VS head, pooled scores off by more than the stated bound, a PE pair
-dropped far from the cut, a PE row without its diagonal."""
+"""CPU checks of the GPU parity helper (tests/parity.py).
+
+A selection that reproduces the oracle's passes, and each kind of mistake the helper
+exists to catch is rejected:
+- VS heads: a changed CSR row; a block dropped from the block set far from the floor, with
+  the CSR rows following it; pooled scores off by more than the stated bound;
+- routing: a route flipped far from tau; a C_struct error;
+- PE heads: a pair dropped far from the cut; a pair added below it; a row without its
+  diagonal;
+- outputs: errors beyond the output tolerances.
+"""
 import numpy as np
 import pytest
 
@@ -103,3 +110,67 @@ def test_near_threshold_counts_grow_with_the_band(tiny):
     for k in a:
         assert 0 <= a[k] <= b[k] <= c[k]
     assert c["near_pe_pairs"] > b["near_pe_pairs"] > 0
+
+
+def test_helper_rejects_a_route_flipped_far_from_tau(tiny):
+    w, g, osel = tiny
+    assert abs(osel[0]["c_struct"] - w.tau_proxy) > 10 * P.TOL_REL * w.tau_proxy
+    sel = _fake_gpu_selection(w, osel)
+    sel["route_vs"][0] = 0
+    with pytest.raises(AssertionError, match="route differs"):
+        P.compare_selection(w, sel, osel, g=g)
+
+
+def test_helper_rejects_c_struct_error(tiny):
+    w, g, osel = tiny
+    sel = _fake_gpu_selection(w, osel)
+    sel["c_struct"][1] += np.float32(1e-3)
+    with pytest.raises(AssertionError, match="C_struct"):
+        P.compare_selection(w, sel, osel, g=g)
+
+
+def test_helper_rejects_a_vs_block_dropped_far_from_the_floor(tiny):
+    """The GPU's own block set loses a block scored far above alpha * mu, and its CSR rows
+    follow that set (so the union rule holds): the block-set comparison must catch it."""
+    w, g, osel = tiny
+    o = osel[0]
+    thr = w.alpha * o["mu_v"]
+    kth = P._kth_largest(o["p_v"], o["k_v"])      # the padding's reference score
+    far = [J for J in o["S_v"] if o["p_v"][J] > 2 * thr and J not in (0, w.n_blocks - 1)
+           and abs(o["p_v"][J] - kth) > 10 * P.TOL_REL * kth]
+    assert far
+    sel = _fake_gpu_selection(w, osel)
+    sel["sel_v"][0, far[0]] = 0
+    m = P.O.vs_block_mask(np.nonzero(sel["sel_v"][0])[0], np.nonzero(sel["sel_s"][0])[0],
+                          w.n_blocks)
+    sel["row_ptr"], sel["col"] = _with_mask(w, osel, 0, m)
+    with pytest.raises(AssertionError, match="differs"):
+        P.compare_selection(w, sel, osel, g=g)
+
+
+def test_helper_rejects_an_extra_pe_pair_below_the_cut(tiny):
+    w, g, osel = tiny
+    o = osel[1]
+    m = o["mask"].copy()
+    v = np.where(np.tril(~m), o["v"], np.inf)
+    I, K = np.unravel_index(int(np.argmin(v)), v.shape)   # the smallest unselected v
+    assert abs(v[I, K] - o["v_star"]) > 10 * P.TOL_REL * o["v_star"]
+    m[I, K] = True
+    sel = _fake_gpu_selection(w, osel)
+    sel["row_ptr"], sel["col"] = _with_mask(w, osel, 1, m)
+    with pytest.raises(AssertionError, match="PE pair"):
+        P.compare_selection(w, sel, osel, g=g)
+
+
+def test_output_tolerances():
+    """compare_outputs holds max abs 2e-2, mean abs 2e-3 and relative RMS 1e-2."""
+    ref = np.random.default_rng(3).standard_normal((256, 128)) / np.sqrt(128)
+    P.compare_outputs(ref + 5e-4, ref, "small uniform error passes")
+    one = ref.copy()
+    one[7, 9] += 3e-2
+    with pytest.raises(AssertionError, match="max abs"):
+        P.compare_outputs(one, ref, "one large error")
+    with pytest.raises(AssertionError):
+        P.compare_outputs(ref + 3e-3, ref, "mean error")
+    with pytest.raises(AssertionError):
+        P.compare_outputs(ref * 1.05, ref, "relative error")
