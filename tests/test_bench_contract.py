@@ -30,3 +30,21 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["sample"] and "VS" in cb["sample"] and "PE" in cb["sample"]
+
+
+def test_algorithmic_flops_counts_causal_token_pairs():
+    """The roofline's numerator: every causal (query, key) token pair of a selected block
+    pair costs one d-long dot product for Q K^T and one d-long multiply-add row for P V,
+    i.e. 4d FLOP ("Prerequisites", A(Q,K,V,S) = Softmax(QK^T/sqrt(d) + M_S) V, causal).
+    Brute force over a random lower-triangular block mask that keeps every diagonal."""
+    import numpy as np
+    import bench
+    B, D, nb = bench.B, bench.D, 6
+    rng = np.random.default_rng(5)
+    mask = np.tril(rng.random((nb, nb)) < 0.5)
+    mask[np.arange(nb), np.arange(nb)] = True
+    tok = np.arange(nb * B)
+    blk = tok // B
+    pairs = (tok[None, :] <= tok[:, None]) & mask[blk[:, None], blk[None, :]]
+    brute = 4.0 * D * int(pairs.sum())
+    assert bench.algorithmic_flops(int(mask.sum()), nb) == brute
